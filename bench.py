@@ -1,0 +1,494 @@
+"""Benchmark: one decoding step's verify + draft-batch rebuild on one GB300 (or N replicas).
+
+A step is sd_verify -> sd_pdraft_expand -> sd_hidden_gather on one batch of synthetic inputs
+already resident in HBM. W warm-up steps, then exactly K timed steps replayed from one CUDA
+graph that rotates over several input sets (their rows together exceed the 129 MB L2), with a
+CUDA event between every pair of kernels. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config b64] [--impl gb300|reference]
+
+--impl reference times the plain CPU oracle (the baseline this library is checked against) on
+the host cores for the same workload and metric.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify+draft-prep requests/s at 1 GB300; achieved HBM GB/s vs roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the verify kernel, from one ncu
+# capture, keyed by workload and by the hash of the kernel source it was taken on (the number is
+# reported only while the source is unchanged).
+MEASURED_TRAFFIC = {}
+
+
+def _src_hash():
+    h = hashlib.sha256()
+    for f in ("sd_verify.cu", "sd_common.cuh"):
+        with open(os.path.join(ROOT, "verify_draft_prep_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(w, a):
+    """Bytes the method must move per step, from the accepted counts a (numpy [B])."""
+    import torch
+
+    B, K, V, H = w.B, w.K, w.V, w.H
+    T = w.temperature.cpu().numpy()
+    greedy = T == 0
+    esz = 4 if w.kind == "probs" else 2
+    a = a.astype(np.int64)
+    scalars = 4 * K + 4 * (K + 2) + 4  # drafts, out_tokens + num_accepted, temperature
+    if w.kind == "probs":
+        rows = np.where(greedy, a + 1, np.where(a < K, 2, 1))
+        gathers = np.where(greedy, 0, 2 * 32 * np.minimum(a + 1, K))
+    else:
+        rows = np.where(greedy, a + 1, (a + 1) + np.minimum(a + 1, K))
+        gathers = np.zeros_like(a)
+    verify = int((rows * esz * V + gathers + scalars).sum())
+    blocks = (2 * K) // w.block_size + 2
+    expand = int((4 * (K + 4) + 4 * blocks + (a + K) * 17 + (K + 1) + 4 * K).sum())
+    gather = int(((a + 1) * 2 * H + (a + K) * 2 * H).sum()) + 2 * H
+    del torch
+    return verify, expand, gather
+
+
+def make_sets(cfg_name, nsets, device, rank):
+    import workloads
+
+    idx = [c["name"] for c in workloads.CONFIGS].index(cfg_name)
+    return [workloads.make(idx, device=device, gen_seed=1000 + idx + 101 * s + 7919 * rank)
+            for s in range(nsets)]
+
+
+def alloc_outputs(w, device):
+    import torch
+
+    B, K, cap = w.B, w.K, w.capacity
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(out_tokens=torch.empty(B, K + 1, **i32), num_accepted=torch.empty(B, **i32),
+                input_ids=torch.empty(cap, **i32), positions=torch.empty(cap, **i32),
+                slot_mapping=torch.empty(cap, **i32), hidden_map=torch.empty(cap, **i32),
+                is_masked=torch.empty(cap, dtype=torch.uint8, device=device),
+                is_rejected=torch.empty(B, K + 1, dtype=torch.uint8, device=device),
+                start_loc=torch.empty(B + 1, **i32), new_token_idx=torch.empty(B, K, **i32),
+                total_out=torch.empty(1, **i32),
+                out_hidden=torch.empty(cap, w.H, dtype=torch.bfloat16, device=device),
+                err=torch.zeros(1, **i32))
+
+
+def launch_step(sd, w, o, stream=None, events=None):
+    if events:
+        events[0].record(stream)
+    sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
+                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream)
+    if events:
+        events[1].record(stream)
+    sd.sd_pdraft_expand(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
+                        w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
+                        o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
+                        o["new_token_idx"], o["total_out"], err=o["err"], stream=stream)
+    if events:
+        events[2].record(stream)
+    sd.sd_hidden_gather(o["total_out"], o["hidden_map"], w.hidden, w.h_shared, o["out_hidden"],
+                        err=o["err"], stream=stream)
+    if events:
+        events[3].record(stream)
+
+
+def run_cpu_baseline(w_host, budget_s=12.0):
+    """Time the oracle (as it stands) on all host cores on one input set: requests/s."""
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    B, K, V = w_host["B"], w_host["K"], w_host["V"]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        if w_host["kind"] == "probs":
+            res = oracle.verify_probs(w_host["target"], w_host["draft"], w_host["drafts"],
+                                      temperature=w_host["temperature"], seed=0, nthreads=cores)
+        else:
+            res = oracle.verify_logits(w_host["target"], w_host["draft"], w_host["drafts"],
+                                       temperature=w_host["temperature"], seed=0,
+                                       nthreads=cores, margins=False)
+        e = oracle.pdraft_expand(res["out_tokens"], res["num_accepted"], w_host["pos0"],
+                                 w_host["block_table"], w_host["block_size"], w_host["mask"])
+        oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], w_host["hidden"],
+                             w_host["h_shared"])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": B * reps / el, "unit": "requests/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} passes over all {B} requests of one input set "
+                      f"(verify + expand + gather), {el:.1f} s"}
+
+
+def host_copy(w):
+    import torch
+
+    B, K, V = w.B, w.K, w.V
+    bits = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    if w.kind == "probs":
+        tgt = w.target.view(B, K + 1, V).cpu().numpy()
+        dft = w.draft.view(B, K, V).cpu().numpy()
+    else:
+        tgt = bits(w.target).reshape(B, K + 1, V)
+        dft = bits(w.draft).reshape(B, K, V)
+    return dict(B=B, K=K, V=V, kind=w.kind, target=tgt, draft=dft,
+                drafts=w.drafts.cpu().numpy(), temperature=w.temperature.cpu().numpy(),
+                pos0=w.pos0.cpu().numpy(), block_table=w.block_table.cpu().numpy(),
+                block_size=w.block_size, mask=w.mask_token_id, hidden=bits(w.hidden),
+                h_shared=bits(w.h_shared))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="b64")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: auto)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    import verify_draft_prep_gb300 as sd
+
+    sd.load()
+    import workloads
+
+    cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
+    w0 = workloads.make(args.config, device=device, gen_seed=1000 + 7919 * rank)
+    nsets = args.sets or 4
+    sets = [w0] + make_sets(args.config, nsets - 1, device, rank + 1)
+    outs = [alloc_outputs(w, device) for w in sets]
+
+    # warm-up (untimed), then algorithmic bytes from each set's accepted counts
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch_step(sd, sets[i % nsets], outs[i % nsets], stream)
+    stream.synchronize()
+    per_set = []
+    for w, o in zip(sets, outs):
+        a = o["num_accepted"].cpu().numpy()
+        per_set.append(algorithmic_bytes(w, a) + (a,))
+    errs = [int(o["err"].item()) for o in outs]
+
+    # one CUDA graph holding all K timed steps, a timing event between every two kernels
+    # (event-record graph nodes); without that support, the verify kernel is timed in a graph
+    # of its own right after the timed region
+    K = args.steps
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+               for _ in range(K)]
+    except TypeError:
+        evs = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for s in range(K):
+                launch_step(sd, sets[s % nsets], outs[s % nsets], stream,
+                            evs[s] if evs else None)
+    graph.replay()  # one untimed replay (graph upload)
+    stream.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    if evs:
+        t_verify = [evs[s][0].elapsed_time(evs[s][1]) for s in range(K)]
+        t_expand = [evs[s][1].elapsed_time(evs[s][2]) for s in range(K)]
+        t_gather = [evs[s][2].elapsed_time(evs[s][3]) for s in range(K)]
+    else:
+        t_verify = [time_verify_only(sd, sets, outs, stream, K) for _ in range(1)]
+        t_expand = t_gather = [float("nan")]
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    B = sets[0].B
+    ms_per_step = total_ms / K
+    value = world * B * K / (total_ms / 1e3)
+    avg_v = float(np.mean(t_verify))
+    bytes_v = float(np.mean([per_set[s % nsets][0] for s in range(K)]))
+    bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(K)]))
+    peak, peak_kind = _peaks()
+    achieved = bytes_v / (avg_v * 1e-3) / 1e9
+    traffic = MEASURED_TRAFFIC.get((args.config, _src_hash()))
+
+    # end to end through the public API: pinned host inputs -> device, step, results -> host
+    e2e = run_e2e(sd, sets[0], device, args.e2e_steps)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(host_copy(sets[0]))
+
+    a_all = np.concatenate([p[3] for p in per_set])
+    info = {
+        "verify_ms": avg_v, "expand_ms": float(np.mean(t_expand)),
+        "gather_ms": float(np.mean(t_gather)), "step_bytes": bytes_all,
+        "step_GBps": bytes_all / (ms_per_step * 1e-3) / 1e9,
+        "mean_accepted": float(a_all.mean()), "err": errs,
+    }
+    print(json.dumps({"info": info}), file=sys.stderr)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "requests/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32"
+            if cfg["kind"] == "probs" else "bf16", "data": "synthetic",
+            "config": {"workload": workloads.config_label(cfg), "B": B, "K": sets[0].K,
+                       "V": sets[0].V, "H": sets[0].H,
+                       "l2": f"{nsets} rotating input sets (rows of all sets "
+                             f"{nsets * sets[0].target.numel() * sets[0].target.element_size() / 1e9:.1f} GB"
+                             f" > 129 MB L2; a set recurs after {nsets - 1} others)",
+                       "timing": "one CUDA graph of all timed steps, events between kernels",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "sd_verify", "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": bytes_v,
+                         "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clk,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def time_verify_only(sd, sets, outs, stream, K):
+    """Average duration of the verify kernel alone, K launches in one graph (ms)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(K):
+                w, o = sets[s % len(sets)], outs[s % len(sets)]
+                sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
+                             temperature=w.temperature, seed=w.seed, err=o["err"],
+                             stream=stream)
+    g.replay()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / K
+
+
+def run_e2e(sd, w, device, steps):
+    """Same metric through the public API with host buffers: each step copies its inputs from
+    pinned host memory, runs the three calls, and reads every result back."""
+    import torch
+
+    ins = {k: getattr(w, k) for k in ("target", "draft", "drafts", "temperature", "pos0",
+                                      "block_table", "hidden", "h_shared")}
+    host = {k: v.cpu().pin_memory() for k, v in ins.items()}
+    dev = {k: torch.empty_like(v) for k, v in ins.items()}
+    o = alloc_outputs(w, device)
+    res_keys = ("out_tokens", "num_accepted", "input_ids", "positions", "slot_mapping",
+                "hidden_map", "is_masked", "is_rejected", "start_loc", "new_token_idx",
+                "total_out", "out_hidden")
+    back = {k: torch.empty(o[k].shape, dtype=o[k].dtype, pin_memory=True) for k in res_keys}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in back.values())
+
+    class W:
+        pass
+
+    wd = W()
+    for k, v in vars(w).items():
+        setattr(wd, k, v)
+    for k, v in dev.items():
+        setattr(wd, k, v)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for k in ins:
+            dev[k].copy_(host[k], non_blocking=True)
+        launch_step(sd, wd, o, stream)
+        for k in res_keys:
+            back[k].copy_(o[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        stream.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            step()
+        e.record(stream)
+        stream.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": w.B / (ms * 1e-3), "unit": "requests/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def run_reference(args, world):
+    """The oracle on the host cores, same workload, metric and unit."""
+    import torch  # noqa: F401
+
+    import workloads
+
+    cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
+    w = workloads.make(args.config, device="cpu")
+    hc = host_copy(w)
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+
+    def step():
+        if hc["kind"] == "probs":
+            res = oracle.verify_probs(hc["target"], hc["draft"], hc["drafts"],
+                                      temperature=hc["temperature"], seed=0, nthreads=cores)
+        else:
+            res = oracle.verify_logits(hc["target"], hc["draft"], hc["drafts"],
+                                       temperature=hc["temperature"], seed=0, nthreads=cores,
+                                       margins=False)
+        e = oracle.pdraft_expand(res["out_tokens"], res["num_accepted"], hc["pos0"],
+                                 hc["block_table"], hc["block_size"], hc["mask"])
+        oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], hc["hidden"],
+                             hc["h_shared"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = w.B * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "requests/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if cfg["kind"] == "probs" else "bf16",
+        "data": "synthetic", "config": {"workload": workloads.config_label(cfg), "B": w.B,
+                                        "K": w.K, "V": w.V, "H": w.H},
+        "cpu_baseline": {"value": value, "unit": "requests/s", "cores": cores, "kind": "oracle",
+                         "sample": f"every step is the full batch of {w.B} requests"},
+        "e2e": {"value": value, "unit": "requests/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * sd.h -- C ABI of the GB300 (sm_103a) speculative-decoding verify and P-EAGLE draft-batch
+ * rebuild library (libsd_gb300.so).
+ *
+ * Three calls make one decoding step's hot path, in this order on one stream:
+ *   sd_verify         lossless verification of K drafts per request (rejection sampling with a
+ *                     residual resample, or greedy argmax at temperature 0);
+ *   sd_pdraft_expand  rebuild of the drafter batch for the next parallel-drafting pass;
+ *   sd_hidden_gather  drafter hidden states from the target's hidden states or h_shared.
+ *
+ * Conventions for every call:
+ *   - Every pointer is a DEVICE pointer owned by the caller. The library allocates nothing and
+ *     keeps no state between calls.
+ *   - Calls only enqueue work on `stream` (a cudaStream_t; 0 = the legacy default stream) and
+ *     never synchronise, so a step can be captured in a CUDA graph.
+ *   - The return value is SD_OK or a negative SD_E_* code for errors the host can see (null
+ *     pointer, bad size, misaligned pointer, launch failure). Nothing is enqueued on error.
+ *   - Data errors found on the device (a draft token outside [0, V), a position the block table
+ *     does not cover, ...) are OR-ed as SD_ERR_* bits into *err (a device int32 the caller
+ *     zeroes; may be NULL). The kernel then takes the documented fallback. No kernel traps,
+ *     asserts or waits on a flag.
+ *
+ * Notation: B requests, K drafts per request (1 <= K <= SD_K_MAX), V vocabulary entries,
+ * H hidden size. Target rows p_0..p_K of request r are rows r*(K+1)+j of `target`; draft rows
+ * q_0..q_{K-1} are rows r*K+j of `draft`; draft d_{j+1} (drafts[r*K+j]) is checked against row j.
+ */
+#ifndef SD_GB300_H
+#define SD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SD_API __attribute__((visibility("default")))
+#else
+#define SD_API
+#endif
+
+#define SD_K_MAX 16
+
+/* host-visible status codes */
+#define SD_OK 0
+#define SD_E_NULL (-1)     /* a required pointer is NULL */
+#define SD_E_SHAPE (-2)    /* a size or stride is out of range */
+#define SD_E_DTYPE (-3)    /* unknown dtype */
+#define SD_E_ALIGN (-4)    /* a pointer or stride breaks the stated alignment */
+#define SD_E_LAUNCH (-5)   /* the CUDA launch failed (cudaGetLastError is left set) */
+#define SD_E_DEVICE (-6)   /* no usable sm_103 device is current */
+
+/* device-side data error bits, OR-ed into *err */
+#define SD_ERR_TOKEN_RANGE 1    /* a draft token outside [0, V): treated as rejected */
+#define SD_ERR_BLOCK_TABLE 2    /* drafter position not covered by the block table: slot -1 */
+#define SD_ERR_NUM_ACCEPTED 4   /* num_accepted outside [0, K]: clamped */
+#define SD_ERR_MAP_RANGE 8      /* hidden_map row >= n_in_rows: h_shared written instead */
+#define SD_ERR_ZERO_ROW 16      /* a race row without a positive key even on p: token 0 */
+#define SD_ERR_TOTAL_RANGE 32   /* total_out outside [0, capacity]: clamped */
+
+/* input kinds for sd_verify */
+#define SD_F32_PROBS 0    /* fp32 probabilities, already at the sampling temperature */
+#define SD_BF16_LOGITS 1  /* bf16 logits; softmax(l / T_r) is taken inside the kernel */
+
+/*
+ * sd_verify -- batched lossless verification of K drafts per request.
+ *
+ * Speculative-decoding explainer (ainews.alishangtian.com), sections "核心思想" (verify K+1
+ * positions, discard after the first rejection, K+1 tokens when all are accepted),
+ * "修正拒绝采样" (accept with probability min(1, p(x)/q(x)); on rejection resample from the
+ * normalised residual max(0, p - q)) and "边界与代价" (temperature 0 must equal greedy decoding).
+ *
+ * Per request r, with T_r = temperature[r] (NULL: every T_r = 1):
+ *   T_r > 0: draft d_{j+1} is accepted iff u_j * Q < P, with P = p_j(d_{j+1}),
+ *            Q = q_j(d_{j+1}), compared exactly in double, and u_j = (w >> 8) * 2^-24 where w
+ *            is word 0 of Philox4x32-10 block (0, j, r, 0) under key (seed lo, seed hi).
+ *            a_r = index of the first rejection, or K. The final token b_r is
+ *              a_r < K:  argmax_x r(x) / E_x, r = max(0, p_{a_r} - q_{a_r}),
+ *              a_r == K: argmax_x max(0, p_K(x)) / E_x   (the bonus token),
+ *            with E_x = fp32(-log(v)) from the double log, v = (w + 0.5) * 2^-32 and w word
+ *            (x & 3) of block (x >> 2, j, r, 1), j the race row. Keys are fp32 quotients for
+ *            SD_F32_PROBS; ties go to the lowest x. If no key of the residual race is
+ *            positive, the race is re-run on p of the same row with the same E_x; if that has
+ *            none either, b_r = 0 and SD_ERR_ZERO_ROW is raised.
+ *   T_r == 0: accept iff d_{j+1} == argmax_x p_j(x) (lowest x on ties); b_r = argmax p_{a_r}.
+ * For SD_BF16_LOGITS, p_j = softmax(l^t_j / T_r) and q_j = softmax(l^d_j / T_r) are formed in
+ * fp32 inside the kernel (results match a double-precision evaluation within the documented
+ * tolerance, not bit for bit); T_r == 0 works on the raw logits (bit-exact).
+ * Rows after the first rejection are never read.
+ *
+ * Arguments:
+ *   B >= 0, 1 <= K <= SD_K_MAX, V >= 1; dtype SD_F32_PROBS or SD_BF16_LOGITS.
+ *   target [B*(K+1) rows, stride ld_t elements], draft [B*K rows, stride ld_d elements]
+ *     (fp32 or bf16 per dtype; ld >= V). Rows whose start is 16-byte aligned are read with
+ *     128-bit loads, other layouts with scalar loads.
+ *   drafts [B, K] int32; temperature [B] fp32 or NULL; seed: Philox key.
+ * Outputs:
+ *   out_tokens [B, K+1] int32: d_1..d_{a_r}, b_r, then -1.
+ *   num_accepted [B] int32: a_r.
+ *   p_at_draft, q_at_draft [B, K] fp32, each may be NULL: P and Q of every examined draft
+ *     j <= min(a_r, K-1) (probabilities; raw target/draft values for T_r == 0; 0 for an
+ *     out-of-range token), -1 for drafts never examined.
+ *   err: see above.
+ */
+SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft,
+              long ld_d, const int32_t* drafts, const float* temperature, uint64_t seed,
+              int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+              int32_t* err, void* stream);
+
+/*
+ * sd_pdraft_expand -- rebuild of the drafter batch for P-EAGLE parallel drafting.
+ *
+ * P-EAGLE blog (vLLM), sections "核心方法" (drafter position i takes the token and hidden state
+ * of position i-1; MASK positions take emb(mask) and h_shared), "并行草稿生成的挑战" (expand ids,
+ * hidden states and positions with MASK slots, bump positions per request, recompute the slot
+ * mapping and per-request start indices), "Triton Kernel" (one pass also emits the rejected-token
+ * mask, the masked-token mask, the new-token indices and the hidden-state mapping) and
+ * "Hidden State 管理" (PADDING_SLOT_ID = -1).
+ *
+ * Request r with a_r = num_accepted[r] gets L_r = a_r + K consecutive drafter slots starting at
+ * start_loc[r] = sum_{r' < r} L_{r'}. Slot j of request r (i = start_loc[r] + j):
+ *   input_ids[i]    = out_tokens[r][j] for j <= a_r (d_1..d_{a_r}, b_r), else mask_token_id
+ *   positions[i]    = pos0[r] + 1 + j          (pos0[r] = position of verify slot 0)
+ *   slot_mapping[i] = block_table[r][pos / block_size] * block_size + pos % block_size, or -1
+ *                     with SD_ERR_BLOCK_TABLE when the table does not cover pos
+ *   hidden_map[i]   = r*(K+1) + j for j <= a_r (target hidden row), else -1 (h_shared)
+ *   is_masked[i]    = (j > a_r)
+ * Slots total_out <= i < capacity are padding: id -1, position 0, slot -1, map -1, mask 0.
+ * is_rejected [B, K+1]: 1 for verify slots 1 <= j <= K with j > a_r, else 0.
+ * new_token_idx [B, K]: start_loc[r] + a_r + k, the slots whose drafter logits become the next
+ *   drafts. start_loc has B+1 entries; start_loc[B] = *total_out = sum_r L_r.
+ * Arguments: B >= 0, 1 <= K <= SD_K_MAX; out_tokens [B, K+1] and num_accepted [B] as written by
+ *   sd_verify; pos0 [B]; block_table [B, max_blocks] int32 (entries < 0 unused);
+ *   block_size >= 1; capacity >= 0 (B*2*K holds every outcome; a smaller capacity truncates
+ *   with SD_ERR_TOTAL_RANGE). Outputs have `capacity` entries (is_masked uint8).
+ */
+SD_API int sd_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
+                     const int32_t* pos0, const int32_t* block_table, int max_blocks,
+                     int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
+                     int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
+                     uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
+                     int32_t* new_token_idx, int32_t* total_out, int32_t* err, void* stream);
+
+/*
+ * sd_hidden_gather -- drafter hidden states.
+ *
+ * P-EAGLE blog (vLLM), section "Hidden State 管理": target hidden states are copied to their
+ * drafter slots and the learned h_shared fills the MASK slots. Written here in gather form:
+ *   out_hidden[i, :] = hidden_map[i] >= 0 ? target_hidden[hidden_map[i], :] : h_shared[:]
+ * for i < *total_out (read on the device, clamped to capacity with SD_ERR_TOTAL_RANGE). Rows
+ * from *total_out on are not written. A map entry >= n_in_rows writes h_shared and raises
+ * SD_ERR_MAP_RANGE. Rows are H bf16 values moved bit for bit; target_hidden has n_in_rows rows
+ * of stride ld_in elements, out_hidden `capacity` rows of stride ld_out (both >= H).
+ */
+SD_API int sd_hidden_gather(int capacity, int H, const int32_t* total_out, const int32_t* hidden_map,
+                     const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared,
+                     void* out_hidden, long ld_out, int32_t* err, void* stream);
+
+/* ---- diagnostics (test support; same conventions) ---- */
+
+/* Philox4x32-10 of n counters ctr[n][4] under key (seed lo, seed hi) -> out[n][4]. */
+SD_API int sd_philox_words(int n, const uint32_t* ctr, uint64_t seed, uint32_t* out, void* stream);
+
+/* The race variates E = fp32(-log((w + 0.5) * 2^-32)) of n words w[n] -> E[n] (the exact path). */
+SD_API int sd_race_E(int n, const uint32_t* w, float* E, void* stream);
+
+/* Worst relative error, over every w in [w_begin, w_begin + count), of the fast approximation
+ * the race filter uses for -log(v) against the exact E above. Writes max_rel[0] (fp32,
+ * caller-zeroed) with atomicMax on the float bits. */
+SD_API int sd_race_E_approx_error(uint32_t w_begin, uint64_t count, float* max_rel, void* stream);
+
+/* Text for a status code (static storage). */
+SD_API const char* sd_status_string(int status);
+
+/* Library version (major * 100 + minor). */
+SD_API int sd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_GB300_H */

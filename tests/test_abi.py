@@ -1,0 +1,61 @@
+"""The C-ABI library loads and exports every entry point include/sd.h declares; host-side
+argument checks answer before any device work (so they run on a machine without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import verify_draft_prep_gb300 as sd
+from conftest import ROOT
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "sd.h")).read()
+    return sorted(set(re.findall(r"^SD_API\s+[\w\s\*]+?\b(sd_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sd.build()
+    return sd.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"sd_verify", "sd_pdraft_expand", "sd_hidden_gather"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(sd.EXPORTED)
+    assert lib.sd_version() == 100
+
+
+def test_internal_symbols_are_hidden(lib):
+    raw = ctypes.CDLL(sd.LIB_PATH)
+    for n in ("sd_verify_launch", "sd_expand_launch", "sd_gather_launch"):
+        with pytest.raises(AttributeError):
+            getattr(raw, n)
+
+
+def test_host_argument_checks(lib):
+    P = None
+    # K out of range, V < 1, ld < V, bad dtype
+    assert lib.sd_verify(1, 0, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, P) == -2
+    assert lib.sd_verify(1, 17, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, P) == -2
+    assert lib.sd_verify(1, 2, 0, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, P) == -2
+    assert lib.sd_verify(1, 2, 10, 0, P, 9, P, 10, P, P, 0, P, P, P, P, P, P) == -2
+    assert lib.sd_verify(1, 2, 10, 7, P, 10, P, 10, P, P, 0, P, P, P, P, P, P) == -3
+    # null rows
+    assert lib.sd_verify(1, 2, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, P) == -1
+    # an empty batch is a no-op
+    assert lib.sd_verify(0, 2, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, P) == 0
+    # expand: block size 0, null outputs
+    assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 0, 0, 4, *([P] * 11)) == -2
+    assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 16, 0, 4, *([P] * 11)) == -1
+    # gather: H < 1, ld < H, odd (misaligned) bf16 pointer
+    assert lib.sd_hidden_gather(4, 0, P, P, P, 8, 1, P, P, 8, P, P) == -2
+    assert lib.sd_hidden_gather(4, 8, P, P, P, 7, 1, P, P, 8, P, P) == -2
+    one = ctypes.c_int32(0)
+    assert lib.sd_hidden_gather(4, 8, ctypes.addressof(one), 16, 17, 8, 1, 32, 64, 8, P, P) == -4
+    assert lib.sd_status_string(-4).decode().startswith("a pointer")

@@ -1,0 +1,169 @@
+"""Python binding of libsd_gb300 (speculative-decoding verify + P-EAGLE draft-batch rebuild).
+
+Argument marshalling only: every call forwards raw device pointers, sizes and the current CUDA
+stream of the tensors' device to the C ABI declared in include/sd.h; all arithmetic runs in the
+library's sm_103a kernels. There is no fallback: if the shared library is missing or fails to
+load, every call raises.
+
+Build the library with ``verify_draft_prep_gb300.build()`` (nvcc, sm_103a).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB as LIB_PATH
+from ._build import build
+
+SD_F32_PROBS = 0
+SD_BF16_LOGITS = 1
+SD_K_MAX = 16
+
+SD_ERR_TOKEN_RANGE = 1
+SD_ERR_BLOCK_TABLE = 2
+SD_ERR_NUM_ACCEPTED = 4
+SD_ERR_MAP_RANGE = 8
+SD_ERR_ZERO_ROW = 16
+SD_ERR_TOTAL_RANGE = 32
+
+EXPORTED = ["sd_verify", "sd_pdraft_expand", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+            "sd_race_E_approx_error", "sd_status_string", "sd_version"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SDError(RuntimeError):
+    pass
+
+
+def load():
+    """Load libsd_gb300.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise SDError(f"{LIB_PATH} is missing: build it with verify_draft_prep_gb300.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, u32, u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint32,
+                                 ctypes.c_uint64)
+        lib.sd_verify.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, P, P, P, P, P, P]
+        lib.sd_verify.restype = i32
+        lib.sd_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32, i32,
+                                         P, P, P, P, P, P, P, P, P, P, P]
+        lib.sd_pdraft_expand.restype = i32
+        lib.sd_hidden_gather.argtypes = [i32, i32, P, P, P, i64, i32, P, P, i64, P, P]
+        lib.sd_hidden_gather.restype = i32
+        lib.sd_philox_words.argtypes = [i32, P, u64, P, P]
+        lib.sd_philox_words.restype = i32
+        lib.sd_race_E.argtypes = [i32, P, P, P]
+        lib.sd_race_E.restype = i32
+        lib.sd_race_E_approx_error.argtypes = [u32, u64, P, P]
+        lib.sd_race_E_approx_error.restype = i32
+        lib.sd_status_string.argtypes = [i32]
+        lib.sd_status_string.restype = ctypes.c_char_p
+        lib.sd_version.argtypes = []
+        lib.sd_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = load().sd_status_string(rc).decode()
+        raise SDError(f"{what} failed: {msg} ({rc})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise SDError("tensors passed to libsd_gb300 must live on the GPU")
+    return t.data_ptr()
+
+
+def _stream(t, stream):
+    import torch
+
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _row_stride(t):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise SDError("row arrays must be 2-D with contiguous rows")
+    return t.stride(0)
+
+
+def sd_verify(target, draft, drafts, out_tokens, num_accepted, temperature=None, seed=0,
+              p_at_draft=None, q_at_draft=None, err=None, stream=None):
+    """Verify K drafts per request (see include/sd.h).
+
+    target: [B*(K+1), V] float32 probabilities or bfloat16 logits; draft: [B*K, V] same dtype;
+    drafts: [B, K] int32; out_tokens: [B, K+1] int32; num_accepted: [B] int32;
+    temperature: [B] float32 or None; p_at_draft / q_at_draft: [B, K] float32 or None;
+    err: [1] int32 or None.
+    """
+    import torch
+
+    B, K = drafts.shape
+    V = target.shape[1]
+    if target.dtype == torch.float32:
+        dtype = SD_F32_PROBS
+    elif target.dtype == torch.bfloat16:
+        dtype = SD_BF16_LOGITS
+    else:
+        raise SDError("target must be float32 probabilities or bfloat16 logits")
+    if draft.dtype != target.dtype or draft.shape[1] != V:
+        raise SDError("draft must match target's dtype and vocabulary")
+    if target.shape[0] != B * (K + 1) or draft.shape[0] != B * K:
+        raise SDError("row counts must be B*(K+1) (target) and B*K (draft)")
+    rc = load().sd_verify(B, K, V, dtype, _ptr(target), _row_stride(target), _ptr(draft),
+                          _row_stride(draft), _ptr(drafts), _ptr(temperature), seed,
+                          _ptr(out_tokens), _ptr(num_accepted), _ptr(p_at_draft),
+                          _ptr(q_at_draft), _ptr(err), _stream(target, stream))
+    _check(rc, "sd_verify")
+
+
+def sd_pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,
+                     input_ids, positions, slot_mapping, hidden_map, is_masked, is_rejected,
+                     start_loc, new_token_idx, total_out, err=None, stream=None):
+    """Rebuild the drafter batch (see include/sd.h). Outputs have `capacity` = len(input_ids)."""
+    B, K1 = out_tokens.shape
+    rc = load().sd_pdraft_expand(
+        B, K1 - 1, _ptr(out_tokens), _ptr(num_accepted), _ptr(pos0), _ptr(block_table),
+        block_table.shape[1], block_size, mask_token_id, input_ids.shape[0], _ptr(input_ids),
+        _ptr(positions), _ptr(slot_mapping), _ptr(hidden_map), _ptr(is_masked),
+        _ptr(is_rejected), _ptr(start_loc), _ptr(new_token_idx), _ptr(total_out), _ptr(err),
+        _stream(start_loc, stream))
+    _check(rc, "sd_pdraft_expand")
+
+
+def sd_hidden_gather(total_out, hidden_map, target_hidden, h_shared, out_hidden, err=None,
+                     stream=None):
+    """Gather drafter hidden states (see include/sd.h). bf16 rows."""
+    cap, H = out_hidden.shape
+    rc = load().sd_hidden_gather(cap, H, _ptr(total_out), _ptr(hidden_map), _ptr(target_hidden),
+                                 _row_stride(target_hidden), target_hidden.shape[0],
+                                 _ptr(h_shared), _ptr(out_hidden), _row_stride(out_hidden),
+                                 _ptr(err), _stream(out_hidden, stream))
+    _check(rc, "sd_hidden_gather")
+
+
+def sd_philox_words(ctr, seed, out, stream=None):
+    rc = load().sd_philox_words(ctr.shape[0], _ptr(ctr), seed, _ptr(out), _stream(ctr, stream))
+    _check(rc, "sd_philox_words")
+
+
+def sd_race_E(w, E, stream=None):
+    rc = load().sd_race_E(w.shape[0], _ptr(w), _ptr(E), _stream(w, stream))
+    _check(rc, "sd_race_E")
+
+
+def sd_race_E_approx_error(w_begin, count, max_rel, stream=None):
+    rc = load().sd_race_E_approx_error(w_begin, count, _ptr(max_rel), _stream(max_rel, stream))
+    _check(rc, "sd_race_E_approx_error")

@@ -1,0 +1,141 @@
+// sd_abi.cu -- the exported C entry points of libsd_gb300: host-side argument checks, then one
+// asynchronous launch on the caller's stream. See include/sd.h for the contract of each call.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sd.h"
+
+extern "C" {
+int sd_verify_launch(int, int, int, int, const void*, long, const void*, long, const int32_t*,
+                     const float*, uint64_t, int32_t*, int32_t*, float*, float*, int32_t*,
+                     cudaStream_t);
+int sd_expand_launch(int, int, const int32_t*, const int32_t*, const int32_t*, const int32_t*,
+                     int, int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*,
+                     uint8_t*, int32_t*, int32_t*, int32_t*, int32_t*, cudaStream_t);
+int sd_gather_launch(int, int, const int32_t*, const int32_t*, const void*, long, int,
+                     const void*, void*, long, int32_t*, cudaStream_t);
+int sd_philox_launch(int, const uint32_t*, uint64_t, uint32_t*, cudaStream_t);
+int sd_race_E_launch(int, const uint32_t*, float*, cudaStream_t);
+int sd_approx_error_launch(uint32_t, uint64_t, float*, cudaStream_t);
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_device_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+
+// The kernels are built for sm_103a only.
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return SD_E_DEVICE;
+  if (dev < kMaxDevices && g_device_ok[dev] != 0) return g_device_ok[dev] > 0 ? SD_OK : SD_E_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SD_E_DEVICE;
+  const int ok = (major == 10 && minor == 3) ? 1 : -1;
+  if (dev < kMaxDevices) g_device_ok[dev] = ok;
+  return ok > 0 ? SD_OK : SD_E_DEVICE;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sd_version(void) { return 100; }
+
+const char* sd_status_string(int status) {
+  switch (status) {
+    case SD_OK: return "ok";
+    case SD_E_NULL: return "a required pointer is NULL";
+    case SD_E_SHAPE: return "a size or stride is out of range";
+    case SD_E_DTYPE: return "unknown dtype";
+    case SD_E_ALIGN: return "a pointer or stride breaks the required alignment";
+    case SD_E_LAUNCH: return "CUDA launch failed";
+    case SD_E_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft,
+              long ld_d, const int32_t* drafts, const float* temperature, uint64_t seed,
+              int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+              int32_t* err, void* stream) {
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
+  if ((long long)B * (K + 1) > 2147483647LL) return SD_E_SHAPE;
+  if (B == 0) return SD_OK;
+  if (!target || !draft || !drafts || !out_tokens || !num_accepted) return SD_E_NULL;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  if ((uintptr_t)target % esize || (uintptr_t)draft % esize) return SD_E_ALIGN;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
+                          out_tokens, num_accepted, p_at_draft, q_at_draft, err,
+                          (cudaStream_t)stream);
+}
+
+int sd_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
+                     const int32_t* pos0, const int32_t* block_table, int max_blocks,
+                     int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
+                     int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
+                     uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
+                     int32_t* new_token_idx, int32_t* total_out, int32_t* err, void* stream) {
+  if (B < 0 || K < 1 || K > SD_K_MAX || max_blocks < 0 || block_size < 1 || capacity < 0)
+    return SD_E_SHAPE;
+  if ((long long)B * 2 * K > 2147483647LL) return SD_E_SHAPE;
+  if (!start_loc || !total_out) return SD_E_NULL;
+  if (B > 0 && (!out_tokens || !num_accepted || !pos0 || !is_rejected || !new_token_idx ||
+                (max_blocks > 0 && !block_table)))
+    return SD_E_NULL;
+  if (capacity > 0 && (!input_ids || !positions || !slot_mapping || !hidden_map || !is_masked))
+    return SD_E_NULL;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_expand_launch(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks,
+                          block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
+                          hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out,
+                          err, (cudaStream_t)stream);
+}
+
+int sd_hidden_gather(int capacity, int H, const int32_t* total_out, const int32_t* hidden_map,
+                     const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared,
+                     void* out_hidden, long ld_out, int32_t* err, void* stream) {
+  if (capacity < 0 || H < 1 || ld_in < H || ld_out < H || n_in_rows < 0) return SD_E_SHAPE;
+  if (!total_out || !h_shared) return SD_E_NULL;
+  if (capacity > 0 && (!hidden_map || !out_hidden)) return SD_E_NULL;
+  if (n_in_rows > 0 && !target_hidden) return SD_E_NULL;
+  if ((uintptr_t)target_hidden % 2 || (uintptr_t)h_shared % 2 || (uintptr_t)out_hidden % 2)
+    return SD_E_ALIGN;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_gather_launch(capacity, H, total_out, hidden_map, target_hidden, ld_in, n_in_rows,
+                          h_shared, out_hidden, ld_out, err, (cudaStream_t)stream);
+}
+
+int sd_philox_words(int n, const uint32_t* ctr, uint64_t seed, uint32_t* out, void* stream) {
+  if (n < 0) return SD_E_SHAPE;
+  if (n > 0 && (!ctr || !out)) return SD_E_NULL;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_philox_launch(n, ctr, seed, out, (cudaStream_t)stream);
+}
+
+int sd_race_E(int n, const uint32_t* w, float* E, void* stream) {
+  if (n < 0) return SD_E_SHAPE;
+  if (n > 0 && (!w || !E)) return SD_E_NULL;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_race_E_launch(n, w, E, (cudaStream_t)stream);
+}
+
+int sd_race_E_approx_error(uint32_t w_begin, uint64_t count, float* max_rel, void* stream) {
+  if (count > (1ull << 32)) return SD_E_SHAPE;
+  if (!max_rel) return SD_E_NULL;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_approx_error_launch(w_begin, count, max_rel, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// sd_diag.cu -- diagnostic kernels: the device Philox stream, the exact race variate, and the
+// exhaustive error bound of the race filter's fast -log approximation.
+
+#include <math.h>
+
+#include "sd_common.cuh"
+
+namespace sdk {
+
+__global__ void philox_kernel(int n, const uint32_t* ctr, PhiloxKey key, uint32_t* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    const uint4 c = make_uint4(ctr[4 * i], ctr[4 * i + 1], ctr[4 * i + 2], ctr[4 * i + 3]);
+    const uint4 o = philox4x32_10(c, key);
+    out[4 * i] = o.x;
+    out[4 * i + 1] = o.y;
+    out[4 * i + 2] = o.z;
+    out[4 * i + 3] = o.w;
+  }
+}
+
+__global__ void race_E_kernel(int n, const uint32_t* w, float* E) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) E[i] = race_E_exact(w[i]);
+}
+
+// max over w of |Ls(w) / (E(w) * log2(e) * 2^64) - 1|, evaluated in double.
+__global__ void approx_error_kernel(uint32_t w_begin, unsigned long long count, float* max_rel) {
+  const double scale = 1.4426950408889634 * 18446744073709551616.0;
+  double worst = 0.0;
+  for (unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+       k < count; k += (unsigned long long)gridDim.x * blockDim.x) {
+    const uint32_t w = (uint32_t)(w_begin + k);
+    const double approx = (double)race_Ls(w);
+    const double exact = (double)race_E_exact(w) * scale;
+    const double rel = fabs(approx / exact - 1.0);
+    worst = rel > worst ? rel : worst;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) worst = fmax(worst, __shfl_xor_sync(0xffffffffu, worst, o));
+  if ((threadIdx.x & 31) == 0) {
+    const float f = (float)worst * 1.0000001f;  // round up
+    atomicMax(reinterpret_cast<int*>(max_rel), __float_as_int(f));
+  }
+}
+
+}  // namespace sdk
+
+extern "C" int sd_philox_launch(int n, const uint32_t* ctr, uint64_t seed, uint32_t* out,
+                                cudaStream_t stream) {
+  if (n == 0) return SD_OK;
+  sdk::philox_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, ctr, sdk::philox_key(seed), out);
+  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}
+
+extern "C" int sd_race_E_launch(int n, const uint32_t* w, float* E, cudaStream_t stream) {
+  if (n == 0) return SD_OK;
+  sdk::race_E_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, w, E);
+  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}
+
+extern "C" int sd_approx_error_launch(uint32_t w_begin, uint64_t count, float* max_rel,
+                                      cudaStream_t stream) {
+  if (count == 0) return SD_OK;
+  sdk::approx_error_kernel<<<152 * 8, 256, 0, stream>>>(w_begin, (unsigned long long)count,
+                                                         max_rel);
+  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}

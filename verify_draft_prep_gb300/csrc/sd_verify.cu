@@ -1,0 +1,772 @@
+// sd_verify.cu -- batched lossless verification of K drafts per request (sm_103a).
+//
+// Speculative-decoding explainer (ainews.alishangtian.com), sections "核心思想" and
+// "修正拒绝采样": accept a draft with probability min(1, p/q), resample the first rejected
+// position from the normalised residual max(0, p - q), emit a bonus token from p_K when every
+// draft is accepted; section "边界与代价": temperature 0 must reproduce greedy decoding.
+//
+// Design (one GB300, HBM-bound):
+//  * One thread-block cluster of CL CTAs per request. Each CTA owns 1/CL of every vocab row; the
+//    CTAs combine row-wide results (argmax keys, softmax statistics) through distributed shared
+//    memory, so a request's rows are visited in order and nothing is read past the first
+//    rejection. No global workspace, no atomics on the data path, no spin-waits.
+//  * Sampled requests on probability rows: the accept scan is K scalar gathers (one lane per
+//    draft); only the one residual (or bonus) row pair is streamed, with 128-bit loads.
+//  * The residual resample is an exponential race argmax_x r(x)/E_x. E_x needs a double log,
+//    which GB300 executes slowly, so each thread filters with an fp32 approximation (one
+//    hardware lg2) and keeps only elements whose approximate key lies within a relative band
+//    of its running best; the CTA then evaluates the exact key r / fp32(-log(v)) for the few
+//    candidates. The band is 16x the exhaustively measured worst error of the approximation,
+//    so the winner (including the lowest-index rule on exact ties) is always among the
+//    candidates.
+//  * Greedy requests scan rows 0..a_r in order, one cluster-wide argmax per row.
+//  * Logit rows (bf16): per row the cluster forms max and sum of exp2((l - M) * log2(e)/T) for
+//    the target and draft rows together, decides the draft, and on rejection races on the same
+//    rows again (the second read is served from L2).
+
+#include <float.h>
+#include <math.h>
+
+#include <type_traits>
+
+#include "sd_common.cuh"
+
+namespace sdk {
+
+constexpr int NT = 256;        // threads per CTA
+constexpr int UNROLL = 4;      // 16-byte units in flight per thread per row
+constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
+constexpr float kBandCand = 1.0f / 512.0f;  // candidate band (relative)
+constexpr float kBandDup = 1.0f / 256.0f;   // in-thread near-tie band (>= candidate band)
+
+struct VerifyParams {
+  int B, K, V;
+  const void* target;
+  long ld_t;
+  const void* draft;
+  long ld_d;
+  const int32_t* drafts;
+  const float* temperature;
+  PhiloxKey key;
+  int32_t* out_tokens;
+  int32_t* num_accepted;
+  float* p_at;
+  float* q_at;
+  int32_t* err;
+  int cl;
+  int vec;  // 1: every row starts on a 16-byte boundary
+};
+
+// ---------------------------------------------------------------------------------- row sources
+// A "unit" is 16 bytes of a row: 4 fp32 or 8 bf16 elements. Units past V (the ragged tail) and
+// rows that are not 16-byte aligned use scalar loads; elements past V take a neutral fill.
+
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+  const uint4 v = ld_stream_u4(p);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                     __uint_as_float(v.w));
+}
+
+__device__ __forceinline__ void f32_unit(const float* row, uint32_t u, uint32_t V, bool vec,
+                                         float fill, float (&v)[4]) {
+  const uint32_t x0 = u * 4u;
+  if (vec && x0 + 4u <= V) {
+    const float4 t = ld_f4(row + x0);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (x0 + i < V) ? __ldg(row + x0 + i) : fill;
+  }
+}
+
+// 8 bf16 values as raw 16-bit words; entries past V read as bf16 -inf (0xff80).
+__device__ __forceinline__ uint4 bf16_raw(const uint16_t* row, uint32_t u, uint32_t V, bool vec) {
+  const uint32_t x0 = u * 8u;
+  if (vec && x0 + 8u <= V) return ld_stream_u4(row + x0);
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = (x0 + i < V) ? (uint32_t)__ldg(row + x0 + i) : 0xff80u;
+  return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                    h[6] | (h[7] << 16));
+}
+
+__device__ __forceinline__ float bf16_at(const uint4& w, int i) {
+  const uint32_t v = (i < 2) ? w.x : (i < 4) ? w.y : (i < 6) ? w.z : w.w;
+  return (i & 1) ? __uint_as_float(v & 0xffff0000u) : __uint_as_float(v << 16);
+}
+
+// Residual (or bonus) values r(x) over fp32 probability rows.
+template <bool HAS_Q>
+struct F32Residual {
+  static constexpr int EPU = 4;
+  const float* p;
+  const float* q;
+  uint32_t V;
+  bool vec;
+  struct Raw {
+    float p[4], q[4];
+  };
+  __device__ __forceinline__ void fetch(uint32_t u, Raw& raw) const {
+    f32_unit(p, u, V, vec, 0.0f, raw.p);
+    if (HAS_Q) f32_unit(q, u, V, vec, 0.0f, raw.q);
+  }
+  __device__ __forceinline__ void residual(const Raw& raw, float (&r)[4]) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = HAS_Q ? __fsub_rn(raw.p[i], raw.q[i]) : raw.p[i];
+  }
+  __device__ __forceinline__ float at(uint32_t x) const {
+    return HAS_Q ? __fsub_rn(__ldg(p + x), __ldg(q + x)) : __ldg(p + x);
+  }
+};
+
+// p(x) = exp2((l - M) * c) / S with c = log2(e) / T, written with explicit roundings so that the
+// streamed pass and the scalar re-evaluation of a candidate give the same bits.
+__device__ __forceinline__ float logit_prob(float l, float M, float c, float invS) {
+  return __fmul_rn(exp2f(__fmul_rn(__fsub_rn(l, M), c)), invS);
+}
+
+template <bool HAS_Q>
+struct Bf16Residual {
+  static constexpr int EPU = 8;
+  const uint16_t* t;
+  const uint16_t* d;
+  float Mt, invSt, Md, invSd, c;
+  uint32_t V;
+  bool vec;
+  struct Raw {
+    uint4 t, d;
+  };
+  __device__ __forceinline__ void fetch(uint32_t u, Raw& raw) const {
+    raw.t = bf16_raw(t, u, V, vec);
+    if (HAS_Q) raw.d = bf16_raw(d, u, V, vec);
+  }
+  __device__ __forceinline__ void residual(const Raw& raw, float (&r)[8]) const {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float pv = logit_prob(bf16_at(raw.t, i), Mt, c, invSt);
+      r[i] = HAS_Q ? __fsub_rn(pv, logit_prob(bf16_at(raw.d, i), Md, c, invSd)) : pv;
+    }
+  }
+  __device__ __forceinline__ float at(uint32_t x) const {
+    const float pv = logit_prob(bf16_bits_to_float(__ldg(t + x)), Mt, c, invSt);
+    return HAS_Q ? __fsub_rn(pv, logit_prob(bf16_bits_to_float(__ldg(d + x)), Md, c, invSd)) : pv;
+  }
+};
+
+// -------------------------------------------------------------------------------- shared state
+struct Smem {
+  uint64_t red[NT / 32];
+  float redf[4][NT / 32];
+  uint64_t slot[2];   // per-CTA cluster exchange (double-buffered)
+  float4 fslot[2];
+  uint64_t bcast;
+  float4 fbcast;
+  float P[SD_K_MAX], Q[SD_K_MAX];
+  int a;
+  int e;
+};
+
+// Cluster-wide maximum of a CTA-uniform value. Every CTA of the cluster calls it the same
+// number of times (control flow is uniform across the cluster by construction).
+__device__ uint64_t cluster_max_u64(uint64_t v, Smem& sm, int& phase, int cl) {
+  if (cl == 1) return v;
+  if (threadIdx.x == 0) sm.slot[phase] = v;
+  cluster_barrier();
+  if (threadIdx.x < 32) {
+    uint64_t m = (threadIdx.x < (unsigned)cl) ? load_from_rank(&sm.slot[phase], threadIdx.x) : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, m, o);
+      m = other > m ? other : m;
+    }
+    if (threadIdx.x == 0) sm.bcast = m;
+  }
+  __syncthreads();
+  const uint64_t m = sm.bcast;
+  phase ^= 1;
+  return m;
+}
+
+// ------------------------------------------------------------------------------------ the race
+struct RaceState {
+  float rb, Lb;   // residual and scaled -log2 of the running best (its key is rb / Lb)
+  uint32_t xb;
+  bool dup;       // another element of this thread lies within kBandDup of the best
+};
+
+__device__ __forceinline__ void race_consider(RaceState& s, float r, float Ls, uint32_t x) {
+  if (r > 0.0f) {
+    const float c = r * s.Lb;  // compares r/Ls against rb/Lb without a division
+    const float d = s.rb * Ls;
+    if (c * (1.0f + kBandDup) >= d) {
+      if (c > d) {
+        s.dup = d * (1.0f + kBandDup) >= c;
+        s.rb = r;
+        s.Lb = Ls;
+        s.xb = x;
+      } else {
+        s.dup = true;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t exact_key(float r, uint32_t w, uint32_t x) {
+  const float key = __fdiv_rn(fmaxf(r, 0.0f), race_E_exact(w));
+  return pack_key(__float_as_uint(key), x);
+}
+
+// Largest approximate key of the CTA, as a (residual, Ls) pair, broadcast to every thread.
+__device__ void block_best_pair(float rb, float Lb, float& rA, float& LA, Smem& sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ro = __shfl_xor_sync(0xffffffffu, rb, o);
+    const float Lo = __shfl_xor_sync(0xffffffffu, Lb, o);
+    if (ro * Lb > rb * Lo) {
+      rb = ro;
+      Lb = Lo;
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) {
+    sm.redf[0][warp] = rb;
+    sm.redf[1][warp] = Lb;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    rb = lane < NT / 32 ? sm.redf[0][lane] : 0.0f;
+    Lb = lane < NT / 32 ? sm.redf[1][lane] : 1.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ro = __shfl_xor_sync(0xffffffffu, rb, o);
+      const float Lo = __shfl_xor_sync(0xffffffffu, Lb, o);
+      if (ro * Lb > rb * Lo) {
+        rb = ro;
+        Lb = Lo;
+      }
+    }
+    if (lane == 0) sm.fbcast = make_float4(rb, Lb, 0.f, 0.f);
+  }
+  __syncthreads();
+  rA = sm.fbcast.x;
+  LA = sm.fbcast.y;
+}
+
+// Exact race winner over units [u0, u1) of one row: returns the CTA's packed (key, ~x) maximum,
+// or 0 when no element of the chunk has a positive residual.
+template <class Src>
+__device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, PhiloxKey key,
+                               uint32_t rid, uint32_t j, Smem& sm) {
+  constexpr int EPU = Src::EPU;
+  RaceState s{0.0f, 1.0f, 0xffffffffu, false};
+  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * UNROLL) {
+    typename Src::Raw raw[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint32_t u = ub + k * NT;
+      if (u < u1) src.fetch(u, raw[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint32_t u = ub + k * NT;
+      if (u < u1) {
+        float r[EPU];
+        src.residual(raw[k], r);
+#pragma unroll
+        for (int h = 0; h < EPU / 4; ++h) {
+          const uint4 w = race_block(key, u * (EPU / 4) + h, rid, j);
+          const uint32_t x0 = u * EPU + 4 * h;
+          race_consider(s, r[4 * h + 0], race_Ls(w.x), x0 + 0);
+          race_consider(s, r[4 * h + 1], race_Ls(w.y), x0 + 1);
+          race_consider(s, r[4 * h + 2], race_Ls(w.z), x0 + 2);
+          race_consider(s, r[4 * h + 3], race_Ls(w.w), x0 + 3);
+        }
+      }
+    }
+  }
+  float rA, LA;
+  block_best_pair(s.rb, s.Lb, rA, LA, sm);
+  uint64_t best = 0ull;
+  if (rA > 0.0f) {
+    // A CTA maximum below about 2^-100 (subnormal territory for the keys): evaluate every
+    // positive element exactly, since fp32 rounding of tiny keys is no longer relative.
+    const bool tiny = !(rA * 0x1p100f >= LA * 0x1p-64f);
+    const bool cand = s.rb > 0.0f && (s.rb * LA * (1.0f + kBandCand) >= rA * s.Lb);
+    if (tiny || (cand && s.dup)) {
+      for (uint32_t u = u0 + threadIdx.x; u < u1; u += NT) {
+        typename Src::Raw raw;
+        src.fetch(u, raw);
+        float r[EPU];
+        src.residual(raw, r);
+#pragma unroll
+        for (int h = 0; h < EPU / 4; ++h) {
+          const uint4 w4 = race_block(key, u * (EPU / 4) + h, rid, j);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float rv = r[4 * h + i];
+            const uint32_t w = word_of(w4, i);
+            if (rv > 0.0f && (tiny || rv * LA * (1.0f + kBandCand) >= rA * race_Ls(w))) {
+              const uint64_t k = exact_key(rv, w, u * EPU + 4 * h + i);
+              best = k > best ? k : best;
+            }
+          }
+        }
+      }
+    } else if (cand) {
+      const uint4 w4 = race_block(key, s.xb >> 2, rid, j);
+      best = exact_key(src.at(s.xb), word_of(w4, s.xb & 3u), s.xb);
+    }
+  }
+  return block_max_u64<NT>(best, sm.red);
+}
+
+// --------------------------------------------------------------------------------- greedy rows
+__device__ __forceinline__ void argmax_take(float v, uint32_t x, float& best, uint32_t& bx) {
+  if (v > best) {
+    best = v;
+    bx = x;
+  }
+}
+
+template <int DT>
+__device__ uint64_t argmax_chunk(const void* row, uint32_t V, bool vec, uint32_t u0, uint32_t u1,
+                                 Smem& sm) {
+  float best = -INFINITY;
+  uint32_t bx = 0xffffffffu;
+  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * UNROLL) {
+    if (DT == SD_F32_PROBS) {
+      float v[UNROLL][4];
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const uint32_t u = ub + k * NT;
+        if (u < u1) f32_unit((const float*)row, u, V, vec, -INFINITY, v[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const uint32_t u = ub + k * NT;
+        if (u < u1) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) argmax_take(v[k][i], u * 4 + i, best, bx);
+        }
+      }
+    } else {
+      uint4 v[UNROLL];
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const uint32_t u = ub + k * NT;
+        if (u < u1) v[k] = bf16_raw((const uint16_t*)row, u, V, vec);
+      }
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        const uint32_t u = ub + k * NT;
+        if (u < u1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v[k], i), u * 8 + i, best, bx);
+        }
+      }
+    }
+  }
+  const uint64_t pk = (bx == 0xffffffffu) ? 0ull : pack_key(orderable(best), bx);
+  return block_max_u64<NT>(pk, sm.red);
+}
+
+// ------------------------------------------------------------------- softmax statistics (bf16)
+struct MaxSum {
+  float m, s;
+};
+
+__device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b, float c) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return MaxSum{m, 0.0f};
+  const float sa = a.m == -INFINITY ? 0.0f : a.s * exp2f((a.m - m) * c);
+  const float sb = b.m == -INFINITY ? 0.0f : b.s * exp2f((b.m - m) * c);
+  return MaxSum{m, sa + sb};
+}
+
+__device__ __forceinline__ void absorb_unit(MaxSum& st, float& comp, const uint4& raw, float c) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = bf16_at(raw, i);
+  float um = v[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) um = fmaxf(um, v[i]);
+  if (um > st.m) {
+    if (st.m != -INFINITY) {
+      const float f = exp2f((st.m - um) * c);
+      st.s *= f;
+      comp *= f;
+    }
+    st.m = um;
+  }
+  if (st.m == -INFINITY) return;
+  float e[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e[i] = exp2f((v[i] - st.m) * c);
+  const float part = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+  // compensated running sum
+  const float y = part - comp;
+  const float t = st.s + y;
+  comp = (t - st.s) - y;
+  st.s = t;
+}
+
+__device__ void block_maxsum2(MaxSum& a, MaxSum& b, float c, Smem& sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MaxSum ao{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+    MaxSum bo{__shfl_xor_sync(0xffffffffu, b.m, o), __shfl_xor_sync(0xffffffffu, b.s, o)};
+    a = combine(a, ao, c);
+    b = combine(b, bo, c);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) {
+    sm.redf[0][warp] = a.m;
+    sm.redf[1][warp] = a.s;
+    sm.redf[2][warp] = b.m;
+    sm.redf[3][warp] = b.s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    a = lane < NT / 32 ? MaxSum{sm.redf[0][lane], sm.redf[1][lane]} : MaxSum{-INFINITY, 0.0f};
+    b = lane < NT / 32 ? MaxSum{sm.redf[2][lane], sm.redf[3][lane]} : MaxSum{-INFINITY, 0.0f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      MaxSum ao{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+      MaxSum bo{__shfl_xor_sync(0xffffffffu, b.m, o), __shfl_xor_sync(0xffffffffu, b.s, o)};
+      a = combine(a, ao, c);
+      b = combine(b, bo, c);
+    }
+    if (lane == 0) sm.fbcast = make_float4(a.m, a.s, b.m, b.s);
+  }
+  __syncthreads();
+  a = MaxSum{sm.fbcast.x, sm.fbcast.y};
+  b = MaxSum{sm.fbcast.z, sm.fbcast.w};
+}
+
+// Row statistics of target row and (if HAS_Q) draft row, combined over the cluster.
+template <bool HAS_Q>
+__device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V, bool vec,
+                          uint32_t u0, uint32_t u1, float c, MaxSum& st, MaxSum& sd, Smem& sm,
+                          int& phase, int cl) {
+  MaxSum a{-INFINITY, 0.0f}, b{-INFINITY, 0.0f};
+  float ca = 0.0f, cb = 0.0f;
+  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * UNROLL) {
+    uint4 vt[UNROLL], vd[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint32_t u = ub + k * NT;
+      if (u < u1) {
+        vt[k] = bf16_raw(trow, u, V, vec);
+        if (HAS_Q) vd[k] = bf16_raw(drow, u, V, vec);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint32_t u = ub + k * NT;
+      if (u < u1) {
+        absorb_unit(a, ca, vt[k], c);
+        if (HAS_Q) absorb_unit(b, cb, vd[k], c);
+      }
+    }
+  }
+  a.s -= ca;
+  b.s -= cb;
+  block_maxsum2(a, b, c, sm);
+  if (cl > 1) {
+    if (threadIdx.x == 0) sm.fslot[phase] = make_float4(a.m, a.s, b.m, b.s);
+    cluster_barrier();
+    if (threadIdx.x == 0) {
+      MaxSum A{-INFINITY, 0.0f}, Bm{-INFINITY, 0.0f};
+      for (int rk = 0; rk < cl; ++rk) {
+        const float4 f = load_from_rank(&sm.fslot[phase], (unsigned)rk);
+        A = combine(A, MaxSum{f.x, f.y}, c);
+        Bm = combine(Bm, MaxSum{f.z, f.w}, c);
+      }
+      sm.fbcast = make_float4(A.m, A.s, Bm.m, Bm.s);
+    }
+    __syncthreads();
+    a = MaxSum{sm.fbcast.x, sm.fbcast.y};
+    b = MaxSum{sm.fbcast.z, sm.fbcast.w};
+    phase ^= 1;
+  }
+  st = a;
+  sd = b;
+}
+
+// ---------------------------------------------------------------------------------- the kernel
+template <int DT>
+__global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
+  __shared__ Smem sm;
+  constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
+  using Elt = typename std::conditional<DT == SD_F32_PROBS, float, uint16_t>::type;
+  const int cl = P.cl;
+  const uint32_t crank = blockIdx.x % (unsigned)cl;
+  const int r = (int)(blockIdx.x / (unsigned)cl);
+  const int K = P.K;
+  const uint32_t V = (uint32_t)P.V;
+  const bool vec = P.vec != 0;
+  const uint32_t NU = (V + EPU - 1) / EPU;
+  const uint32_t u0 = (uint32_t)(((uint64_t)NU * crank) / (unsigned)cl);
+  const uint32_t u1 = (uint32_t)(((uint64_t)NU * (crank + 1)) / (unsigned)cl);
+  const Elt* tbase = (const Elt*)P.target + (size_t)r * (K + 1) * P.ld_t;
+  const Elt* dbase = (const Elt*)P.draft + (size_t)r * K * P.ld_d;
+  auto trow = [&](int j) { return tbase + (size_t)j * P.ld_t; };
+  auto drow = [&](int j) { return dbase + (size_t)j * P.ld_d; };
+  const int32_t* dr = P.drafts + (size_t)r * K;
+  const float T = P.temperature ? P.temperature[r] : 1.0f;
+  const bool greedy = (T == 0.0f);
+  int phase = 0;
+  int a = K;
+  uint32_t b = 0;
+  int32_t e = 0;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x < SD_K_MAX) {
+    sm.P[threadIdx.x] = -1.0f;
+    sm.Q[threadIdx.x] = -1.0f;
+  }
+  __syncthreads();
+
+  if (greedy) {
+    // ---- temperature 0: accept while the draft is the row's argmax (lowest index on ties)
+    for (int j = 0; j <= K; ++j) {
+      const uint64_t pk =
+          cluster_max_u64(argmax_chunk<DT>(trow(j), V, vec, u0, u1, sm), sm, phase, cl);
+      const uint32_t am = packed_index(pk);
+      if (j == K) {
+        b = am;
+        break;
+      }
+      const int d = __ldg(dr + j);
+      const bool valid = d >= 0 && (uint32_t)d < V;
+      if (threadIdx.x == 0) {
+        if (valid) {
+          if (DT == SD_F32_PROBS) {
+            sm.P[j] = __ldg((const float*)trow(j) + d);
+            sm.Q[j] = __ldg((const float*)drow(j) + d);
+          } else {
+            sm.P[j] = bf16_bits_to_float(__ldg((const uint16_t*)trow(j) + d));
+            sm.Q[j] = bf16_bits_to_float(__ldg((const uint16_t*)drow(j) + d));
+          }
+        } else {
+          sm.P[j] = 0.0f;
+          sm.Q[j] = 0.0f;
+        }
+      }
+      if (!valid) e |= SD_ERR_TOKEN_RANGE;
+      if (!valid || (uint32_t)d != am) {
+        a = j;
+        b = am;
+        break;
+      }
+    }
+  } else if (DT == SD_F32_PROBS) {
+    // ---- sampled, probability rows: scalar accept scan, then one race row
+    if (threadIdx.x < 32) {
+      const int j = lane;
+      bool acc = false;
+      bool bad = false;
+      float Pv = 0.0f, Qv = 0.0f;
+      if (j < K) {
+        const int d = __ldg(dr + j);
+        if (d >= 0 && (uint32_t)d < V) {
+          Pv = __ldg((const float*)trow(j) + d);
+          Qv = __ldg((const float*)drow(j) + d);
+          const double u = accept_uniform(P.key, (uint32_t)r, (uint32_t)j);
+          acc = u * (double)Qv < (double)Pv;  // u*Q is exact in double
+        } else {
+          bad = true;
+        }
+      }
+      const unsigned rej = __ballot_sync(0xffffffffu, j < K && !acc);
+      const int av = rej ? __ffs(rej) - 1 : K;
+      if (j < K && j <= av) {
+        sm.P[j] = Pv;
+        sm.Q[j] = Qv;
+      }
+      const unsigned badm = __ballot_sync(0xffffffffu, bad && j == av);
+      if (lane == 0) {
+        sm.a = av;
+        sm.e = badm ? SD_ERR_TOKEN_RANGE : 0;
+      }
+    }
+    __syncthreads();
+    a = sm.a;
+    e = sm.e;
+    const int jr = a < K ? a : K;
+    uint64_t pk;
+    if (a < K) {
+      F32Residual<true> src{(const float*)trow(jr), (const float*)drow(jr), V, vec};
+      pk = cluster_max_u64(race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)jr, sm), sm,
+                           phase, cl);
+    } else {
+      pk = 0ull;
+    }
+    if (packed_key_bits(pk) == 0u) {  // bonus race, or no positive residual key: race on p
+      F32Residual<false> src{(const float*)trow(jr), nullptr, V, vec};
+      pk = cluster_max_u64(race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)jr, sm), sm,
+                           phase, cl);
+    }
+    if (packed_key_bits(pk) == 0u) {
+      e |= SD_ERR_ZERO_ROW;
+      b = 0;
+    } else {
+      b = packed_index(pk);
+    }
+  } else {
+    // ---- sampled, bf16 logit rows: per row max/sum, decide, race on the rejected row
+    const float c = 1.4426950408889634f / T;
+    const uint16_t* t16 = (const uint16_t*)tbase;
+    const uint16_t* d16 = (const uint16_t*)dbase;
+    int jr = K;
+    bool done = false;
+    for (int j = 0; j < K; ++j) {
+      const int d = __ldg(dr + j);
+      const bool valid = d >= 0 && (uint32_t)d < V;
+      MaxSum st, sd;
+      row_stats<true>(t16 + (size_t)j * P.ld_t, d16 + (size_t)j * P.ld_d, V, vec, u0, u1, c, st,
+                      sd, sm, phase, cl);
+      bool accept = false;
+      float Pv = 0.0f, Qv = 0.0f;
+      if (valid) {
+        Pv = __fdiv_rn(exp2f(__fmul_rn(__fsub_rn(bf16_bits_to_float(
+                                                      __ldg(t16 + (size_t)j * P.ld_t + d)),
+                                                  st.m),
+                                        c)),
+                       st.s);
+        Qv = __fdiv_rn(exp2f(__fmul_rn(__fsub_rn(bf16_bits_to_float(
+                                                      __ldg(d16 + (size_t)j * P.ld_d + d)),
+                                                  sd.m),
+                                        c)),
+                       sd.s);
+        const double u = accept_uniform(P.key, (uint32_t)r, (uint32_t)j);
+        accept = u * (double)Qv < (double)Pv;
+      } else {
+        e |= SD_ERR_TOKEN_RANGE;
+      }
+      if (threadIdx.x == 0) {
+        sm.P[j] = Pv;
+        sm.Q[j] = Qv;
+      }
+      if (!accept) {
+        a = j;
+        jr = j;
+        Bf16Residual<true> src{t16 + (size_t)j * P.ld_t, d16 + (size_t)j * P.ld_d, st.m,
+                               1.0f / st.s, sd.m, 1.0f / sd.s, c, V, vec};
+        uint64_t pk = cluster_max_u64(
+            race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)j, sm), sm, phase, cl);
+        if (packed_key_bits(pk) == 0u) {
+          Bf16Residual<false> srcp{t16 + (size_t)j * P.ld_t, nullptr, st.m, 1.0f / st.s,
+                                   0.0f, 0.0f, c, V, vec};
+          pk = cluster_max_u64(race_chunk(srcp, u0, u1, P.key, (uint32_t)r, (uint32_t)j, sm),
+                               sm, phase, cl);
+        }
+        if (packed_key_bits(pk) == 0u) {
+          e |= SD_ERR_ZERO_ROW;
+          b = 0;
+        } else {
+          b = packed_index(pk);
+        }
+        done = true;
+        break;
+      }
+    }
+    if (!done) {
+      MaxSum st, sd;
+      row_stats<false>(t16 + (size_t)jr * P.ld_t, nullptr, V, vec, u0, u1, c, st, sd, sm, phase,
+                       cl);
+      Bf16Residual<false> src{t16 + (size_t)jr * P.ld_t, nullptr, st.m, 1.0f / st.s,
+                              0.0f, 0.0f, c, V, vec};
+      const uint64_t pk = cluster_max_u64(
+          race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)jr, sm), sm, phase, cl);
+      if (packed_key_bits(pk) == 0u) {
+        e |= SD_ERR_ZERO_ROW;
+        b = 0;
+      } else {
+        b = packed_index(pk);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (crank == 0) {
+    const int t = threadIdx.x;
+    if (t <= K) {
+      int32_t tok = -1;
+      if (t < a) tok = __ldg(dr + t);
+      else if (t == a) tok = (int32_t)b;
+      P.out_tokens[(size_t)r * (K + 1) + t] = tok;
+    }
+    if (t < K) {
+      if (P.p_at) P.p_at[(size_t)r * K + t] = sm.P[t];
+      if (P.q_at) P.q_at[(size_t)r * K + t] = sm.Q[t];
+    }
+    if (t == 0) {
+      P.num_accepted[r] = a;
+      raise_err(P.err, e);
+    }
+  }
+  if (cl > 1) cluster_barrier();  // peers may still read this CTA's shared memory
+}
+
+}  // namespace sdk
+
+// ------------------------------------------------------------------------------------ launcher
+namespace {
+
+int choose_cluster(int V, int epu) {
+  const long units = ((long)V + epu - 1) / epu;
+  int cl = sdk::CL_MAX;
+  while (cl > 1 && units / cl < (long)sdk::NT * 2) cl >>= 1;
+  return cl;
+}
+
+}  // namespace
+
+extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* target, long ld_t,
+                                const void* draft, long ld_d, const int32_t* drafts,
+                                const float* temperature, uint64_t seed, int32_t* out_tokens,
+                                int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+                                int32_t* err, cudaStream_t stream) {
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  const int epu = dtype == SD_F32_PROBS ? 4 : 8;
+  sdk::VerifyParams P;
+  P.B = B;
+  P.K = K;
+  P.V = V;
+  P.target = target;
+  P.ld_t = ld_t;
+  P.draft = draft;
+  P.ld_d = ld_d;
+  P.drafts = drafts;
+  P.temperature = temperature;
+  P.key = sdk::philox_key(seed);
+  P.out_tokens = out_tokens;
+  P.num_accepted = num_accepted;
+  P.p_at = p_at_draft;
+  P.q_at = q_at_draft;
+  P.err = err;
+  P.cl = choose_cluster(V, epu);
+  P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
+          ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
+  if (B == 0) return SD_OK;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long)B * P.cl), 1, 1);
+  cfg.blockDim = dim3(sdk::NT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P.cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t rc;
+  if (dtype == SD_F32_PROBS) rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_F32_PROBS>, P);
+  else rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_BF16_LOGITS>, P);
+  return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}
