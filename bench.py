@@ -260,7 +260,7 @@ def main():
 
     cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
     w0 = workloads.make(args.config, device=device, gen_seed=1000 + 7919 * rank)
-    nsets = args.sets or 4
+    nsets = args.sets or (4 if cfg["B"] * cfg["V"] < 64 * 201088 * 2 else 2)
     sets = [w0] + make_sets(args.config, nsets - 1, device, rank + 1)
     outs = [alloc_outputs(w, device) for w in sets]
 
@@ -291,7 +291,8 @@ def main():
             for s in range(K):
                 launch_step(sd, sets[s % nsets], outs[s % nsets], stream,
                             evs[s] if evs else None)
-    graph.replay()  # one untimed replay (graph upload)
+    with torch.cuda.stream(stream):
+        graph.replay()  # one untimed replay (graph upload)
     stream.synchronize()
 
     clocks = ClockSampler(local)
@@ -301,9 +302,10 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    graph.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):  # the graph replays on the current stream
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -383,12 +385,14 @@ def time_verify_only(sd, sets, outs, stream, K):
                 sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
                              temperature=w.temperature, seed=w.seed, err=o["err"],
                              stream=stream)
-    g.replay()
+    with torch.cuda.stream(stream):
+        g.replay()
     stream.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    g.replay()
-    b.record(stream)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        g.replay()
+        b.record(stream)
     stream.synchronize()
     return a.elapsed_time(b) / K
 

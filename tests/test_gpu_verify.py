@@ -100,7 +100,7 @@ def test_lossless_workload_million_requests():
     Q = np.array([[0.10, 0.25, 0.15, 0.10, 0.05, 0.15, 0.10, 0.10],
                   [0.20, 0.10, 0.20, 0.10, 0.10, 0.10, 0.10, 0.10]], np.float32)
     rng = np.random.default_rng(13)
-    drafts = np.stack([rng.choice(V, size=N, p=Q[j].astype(np.float64) / Q[j].sum())
+    drafts = np.stack([rng.choice(V, size=N, p=Q[j].astype(np.float64) / Q[j].astype(np.float64).sum())
                        for j in range(K)], 1).astype(np.int32)
     target = np.ascontiguousarray(np.broadcast_to(P, (N, K + 1, V))).reshape(N * (K + 1), V)
     draft = np.ascontiguousarray(np.broadcast_to(Q, (N, K, V))).reshape(N * K, V)
