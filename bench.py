@@ -1,9 +1,10 @@
 """Benchmark: one decoding step's verify + draft-batch rebuild on one GB300 (or N replicas).
 
-A step is sd_verify -> sd_pdraft_expand -> sd_hidden_gather on one batch of synthetic inputs
-already resident in HBM. W warm-up steps, then exactly K timed steps replayed from one CUDA
-graph that rotates over several input sets (their rows together exceed the 129 MB L2), with a
-CUDA event between every pair of kernels. Prints one JSON line (rank 0).
+A step is sd_verify followed by sd_pdraft_prepare (the draft-batch rebuild and the hidden-state
+gather, launched as a programmatic dependent of verify) on one batch of synthetic inputs already
+resident in HBM. W warm-up steps, then exactly K timed steps replayed from CUDA graphs that rotate
+over several input sets (whose rows together exceed the 129 MB L2). Prints one JSON line
+(rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config b64] [--impl gb300|reference]
 
@@ -55,7 +56,7 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms in the background."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms in the background."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -70,7 +71,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -157,23 +158,51 @@ def alloc_outputs(w, device):
                 err=torch.zeros(1, **i32))
 
 
-def launch_step(sd, w, o, stream=None, events=None):
-    if events:
-        events[0].record(stream)
+def launch_step(sd, w, o, stream=None):
+    """One step: verify, then the fused draft-batch rebuild + hidden gather (a programmatic
+    dependent launch of verify)."""
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
                  temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream)
-    if events:
-        events[1].record(stream)
-    sd.sd_pdraft_expand(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
-                        w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
-                        o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
-                        o["new_token_idx"], o["total_out"], err=o["err"], stream=stream)
-    if events:
-        events[2].record(stream)
-    sd.sd_hidden_gather(o["total_out"], o["hidden_map"], w.hidden, w.h_shared, o["out_hidden"],
-                        err=o["err"], stream=stream)
-    if events:
-        events[3].record(stream)
+    sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
+                         w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
+                         o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
+                         o["new_token_idx"], o["total_out"], w.hidden, w.h_shared,
+                         o["out_hidden"], err=o["err"], stream=stream)
+
+
+def launch_prepare(sd, w, o, stream=None):
+    sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
+                         w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
+                         o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
+                         o["new_token_idx"], o["total_out"], w.hidden, w.h_shared,
+                         o["out_hidden"], err=o["err"], stream=stream)
+
+
+def launch_verify(sd, w, o, stream=None):
+    sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
+                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream)
+
+
+def time_graph(fn, sets, outs, stream, K):
+    """Average duration (ms) of K launches of `fn`, rotating over the input sets, replayed
+    from one CUDA graph."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(K):
+                fn(sets[s % len(sets)], outs[s % len(sets)], stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / K
 
 
 def run_cpu_baseline(w_host, budget_s=12.0):
@@ -225,7 +254,7 @@ def host_copy(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="b64")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -276,24 +305,37 @@ def main():
         per_set.append(algorithmic_bytes(w, a) + (a,))
     errs = [int(o["err"].item()) for o in outs]
 
-    # one CUDA graph holding all K timed steps, a timing event between every two kernels
-    # (event-record graph nodes); without that support, the verify kernel is timed in a graph
-    # of its own right after the timed region
+    # the timed steps are replayed from CUDA graphs of up to CHUNK steps (a graph of K % CHUNK
+    # steps makes up the rest, so exactly K steps run); a timing event (an event-record graph
+    # node) sits at every step boundary, never between the two kernels of a step (that would
+    # break the programmatic launch edge)
     K = args.steps
-    try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-               for _ in range(K)]
-    except TypeError:
-        evs = None
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            for s in range(K):
-                launch_step(sd, sets[s % nsets], outs[s % nsets], stream,
-                            evs[s] if evs else None)
-    with torch.cuda.stream(stream):
-        graph.replay()  # one untimed replay (graph upload)
-    stream.synchronize()
+    CHUNK = min(K, 200)
+
+    def capture(n, with_events):
+        evs_ = None
+        if with_events:
+            try:
+                evs_ = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n + 1)]
+            except TypeError:
+                evs_ = None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for s in range(n):
+                    if evs_:
+                        evs_[s].record(stream)
+                    launch_step(sd, sets[s % nsets], outs[s % nsets], stream)
+                if evs_:
+                    evs_[n].record(stream)
+        with torch.cuda.stream(stream):
+            g.replay()  # one untimed replay (graph upload)
+        stream.synchronize()
+        return g, evs_
+
+    graph, evs = capture(CHUNK, True)
+    full, rest = divmod(K, CHUNK)
+    graph_rest = capture(rest, False)[0] if rest else None
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -302,22 +344,22 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):  # the graph replays on the current stream
+    with torch.cuda.stream(stream):  # graphs replay on the current stream
         start.record(stream)
-        graph.replay()
+        for _ in range(full):
+            graph.replay()
+        if graph_rest is not None:
+            graph_rest.replay()
         end.record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    if evs:
-        t_verify = [evs[s][0].elapsed_time(evs[s][1]) for s in range(K)]
-        t_expand = [evs[s][1].elapsed_time(evs[s][2]) for s in range(K)]
-        t_gather = [evs[s][2].elapsed_time(evs[s][3]) for s in range(K)]
-    else:
-        t_verify = [time_verify_only(sd, sets, outs, stream, K) for _ in range(1)]
-        t_expand = t_gather = [float("nan")]
+    step_ms = [evs[s].elapsed_time(evs[s + 1]) for s in range(CHUNK)] if evs else []
+    # the dominant kernel alone, K launches in a graph of its own, right after the timed region
+    avg_v = time_graph(lambda w, o, st: launch_verify(sd, w, o, st), sets, outs, stream, CHUNK)
+    avg_p = time_graph(lambda w, o, st: launch_prepare(sd, w, o, st), sets, outs, stream, CHUNK)
     if world > 1:
         t = torch.tensor([total_ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -326,9 +368,8 @@ def main():
     B = sets[0].B
     ms_per_step = total_ms / K
     value = world * B * K / (total_ms / 1e3)
-    avg_v = float(np.mean(t_verify))
-    bytes_v = float(np.mean([per_set[s % nsets][0] for s in range(K)]))
-    bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(K)]))
+    bytes_v = float(np.mean([per_set[s % nsets][0] for s in range(CHUNK)]))
+    bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(CHUNK)]))
     peak, peak_kind = _peaks()
     achieved = bytes_v / (avg_v * 1e-3) / 1e9
     traffic = MEASURED_TRAFFIC.get((args.config, _src_hash()))
@@ -342,8 +383,9 @@ def main():
 
     a_all = np.concatenate([p[3] for p in per_set])
     info = {
-        "verify_ms": avg_v, "expand_ms": float(np.mean(t_expand)),
-        "gather_ms": float(np.mean(t_gather)), "step_bytes": bytes_all,
+        "verify_ms": avg_v, "prepare_ms": avg_p,
+        "step_ms_median": float(np.median(step_ms)) if step_ms else None,
+        "step_bytes": bytes_all,
         "step_GBps": bytes_all / (ms_per_step * 1e-3) / 1e9,
         "mean_accepted": float(a_all.mean()), "err": errs,
     }
@@ -359,42 +401,20 @@ def main():
                        "l2": f"{nsets} rotating input sets (rows of all sets "
                              f"{nsets * sets[0].target.numel() * sets[0].target.element_size() / 1e9:.1f} GB"
                              f" > 129 MB L2; a set recurs after {nsets - 1} others)",
-                       "timing": "one CUDA graph of all timed steps, events between kernels",
+                       "timing": "one CUDA graph of all timed steps (verify, then the fused "
+                                 "rebuild as its programmatic dependent); the verify kernel "
+                                 "alone in a second graph for the roofline",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "sd_verify", "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": bytes_v,
                          "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 3 * K, "clocks": clk,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clk,
         }
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
-
-
-def time_verify_only(sd, sets, outs, stream, K):
-    """Average duration of the verify kernel alone, K launches in one graph (ms)."""
-    import torch
-
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(g, stream=stream):
-            for s in range(K):
-                w, o = sets[s % len(sets)], outs[s % len(sets)]
-                sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
-                             temperature=w.temperature, seed=w.seed, err=o["err"],
-                             stream=stream)
-    with torch.cuda.stream(stream):
-        g.replay()
-    stream.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-    stream.synchronize()
-    return a.elapsed_time(b) / K
 
 
 def run_e2e(sd, w, device, steps):

@@ -143,6 +143,26 @@ SD_API int sd_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32
                      int32_t* new_token_idx, int32_t* total_out, int32_t* err, void* stream);
 
 /*
+ * sd_pdraft_prepare -- sd_pdraft_expand and the hidden-state gather of sd_hidden_gather in one
+ * launch: every output of sd_pdraft_expand, plus out_hidden[i, :] for i < total_out (clamped to
+ * capacity) = target_hidden[hidden_map[i], :], or h_shared[:] where hidden_map[i] == -1, as
+ * sd_hidden_gather defines it (same sources: P-EAGLE blog, "Hidden State 管理"). Rows from
+ * total_out on are not written. Arguments are those of the two calls; target_hidden has n_in_rows
+ * rows of stride ld_in, out_hidden `capacity` rows of stride ld_out (both >= H), bf16.
+ * When enqueued right after sd_verify it is launched as a programmatic dependent of it: it is
+ * scheduled while sd_verify drains and waits on the device for sd_verify's results.
+ */
+SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
+                             const int32_t* pos0, const int32_t* block_table, int max_blocks,
+                             int block_size, int32_t mask_token_id, int capacity,
+                             int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
+                             int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
+                             int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out,
+                             int H, const void* target_hidden, long ld_in, int n_in_rows,
+                             const void* h_shared, void* out_hidden, long ld_out, int32_t* err,
+                             void* stream);
+
+/*
  * sd_hidden_gather -- drafter hidden states.
  *
  * P-EAGLE blog (vLLM), section "Hidden State 管理": target hidden states are copied to their

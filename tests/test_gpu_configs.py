@@ -43,7 +43,20 @@ def run_step(w):
                         o["new_token_idx"], o["total_out"], err=o["err"])
     sd.sd_hidden_gather(o["total_out"], o["hidden_map"], w.hidden, w.h_shared, o["out_hidden"],
                         err=o["err"])
+    # the fused rebuild (the benchmark's path) must write the same bytes
+    p = {k: torch.full_like(o[k], 77) for k in ("input_ids", "positions", "slot_mapping",
+                                                  "hidden_map", "is_masked", "is_rejected",
+                                                  "start_loc", "new_token_idx", "total_out")}
+    p_hidden = torch.full((cap, w.H), 7.0, device=dev).to(torch.bfloat16)
+    sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
+                         w.mask_token_id, p["input_ids"], p["positions"], p["slot_mapping"],
+                         p["hidden_map"], p["is_masked"], p["is_rejected"], p["start_loc"],
+                         p["new_token_idx"], p["total_out"], w.hidden, w.h_shared, p_hidden,
+                         err=o["err"])
     torch.cuda.synchronize()
+    for k, v in p.items():
+        assert torch.equal(v, o[k]), k
+    assert torch.equal(p_hidden.view(torch.int16), o["out_hidden"].view(torch.int16))
     res = {k: v.cpu() for k, v in o.items()}
     res = {k: (v.numpy() if v.dtype != torch.bfloat16 else v) for k, v in res.items()}
     res["err"] = int(res["err"][0])

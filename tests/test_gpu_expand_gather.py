@@ -151,3 +151,73 @@ def test_gather_strided_and_map_errors():
                                       out_init=bits(init))
     assert err == werr == oracle.ERR_MAP_RANGE
     assert np.array_equal(bits(got), want)
+
+
+def run_prepare(out_tokens, num_acc, pos0, table, bs, mask_id, target, h_shared, out_init,
+                capacity=None, after_verify=False):
+    """sd_pdraft_prepare (expand + gather in one launch); returns expand outputs and hidden."""
+    B, K1 = out_tokens.shape
+    K = K1 - 1
+    cap = B * 2 * K if capacity is None else capacity
+    dev = "cuda"
+    o = dict(input_ids=torch.full((cap,), 555, dtype=torch.int32, device=dev),
+             positions=torch.full((cap,), 555, dtype=torch.int32, device=dev),
+             slot_mapping=torch.full((cap,), 555, dtype=torch.int32, device=dev),
+             hidden_map=torch.full((cap,), 555, dtype=torch.int32, device=dev),
+             is_masked=torch.full((cap,), 9, dtype=torch.uint8, device=dev),
+             is_rejected=torch.full((B, K + 1), 9, dtype=torch.uint8, device=dev),
+             start_loc=torch.full((B + 1,), 555, dtype=torch.int32, device=dev),
+             new_token_idx=torch.full((B, K), 555, dtype=torch.int32, device=dev),
+             total_out=torch.full((1,), 555, dtype=torch.int32, device=dev))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = out_init.clone().cuda()
+    t = lambda a: torch.as_tensor(np.ascontiguousarray(a, np.int32)).cuda()  # noqa: E731
+    sd.sd_pdraft_prepare(t(out_tokens), t(num_acc), t(pos0), t(table), bs, mask_id,
+                         o["input_ids"], o["positions"], o["slot_mapping"], o["hidden_map"],
+                         o["is_masked"], o["is_rejected"], o["start_loc"], o["new_token_idx"],
+                         o["total_out"], target.cuda(), h_shared.cuda(), out, err=err)
+    torch.cuda.synchronize()
+    res = {k: v.cpu().numpy() for k, v in o.items()}
+    res["err"] = int(err.item())
+    return res, out.cpu()
+
+
+@pytest.mark.parametrize("B,K,H", [(1, 4, 64), (64, 5, 2880), (256, 7, 2048), (300, 8, 2880),
+                                   (1024, 8, 2880), (9, 3, 100), (5, 2, 13), (3000, 16, 64)])
+def test_prepare_bit_exact(B, K, H):
+    rng = np.random.default_rng(B + 7 * K + H)
+    out_tokens, a, pos0, table = _random(rng, B, K)
+    cap = B * 2 * K
+    target = torch.randn(B * (K + 1), H).to(torch.bfloat16)
+    h_shared = torch.randn(H).to(torch.bfloat16)
+    init = torch.full((cap, H), 3.0).to(torch.bfloat16)
+    got, hid = run_prepare(out_tokens, a, pos0, table, 16, 201088, target, h_shared, init)
+    want = oracle.pdraft_expand(out_tokens, a, pos0, table, 16, 201088)
+    check_expand(got, want)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    wh, werr = oracle.hidden_gather(int(want["total_out"][0]), want["hidden_map"], bits(target),
+                                    bits(h_shared), out_init=bits(init))
+    assert werr == 0
+    assert np.array_equal(bits(hid), wh)
+
+
+def test_prepare_errors_and_truncation():
+    rng = np.random.default_rng(77)
+    B, K, H = 300, 4, 24
+    out_tokens, a, pos0, table = _random(rng, B, K)
+    a[7] = 9
+    table[10, :] = -1
+    pos0[11] = -40
+    target = torch.randn(B * (K + 1), H).to(torch.bfloat16)
+    h_shared = torch.randn(H).to(torch.bfloat16)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    for cap in (B * 2 * K, 1000, 0):
+        init = torch.full((cap, H), 3.0).to(torch.bfloat16)
+        got, hid = run_prepare(out_tokens, a, pos0, table, 16, 5, target, h_shared, init,
+                               capacity=cap)
+        want = oracle.pdraft_expand(out_tokens, a, pos0, table, 16, 5, capacity=cap)
+        check_expand(got, want)
+        wh, _ = oracle.hidden_gather(min(int(want["total_out"][0]), cap), want["hidden_map"],
+                                     bits(target), bits(h_shared), capacity=cap,
+                                     out_init=bits(init))
+        assert np.array_equal(bits(hid), wh)

@@ -28,7 +28,7 @@ SD_ERR_MAP_RANGE = 8
 SD_ERR_ZERO_ROW = 16
 SD_ERR_TOTAL_RANGE = 32
 
-EXPORTED = ["sd_verify", "sd_pdraft_expand", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+EXPORTED = ["sd_verify", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -55,6 +55,10 @@ def load():
         lib.sd_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32, i32,
                                          P, P, P, P, P, P, P, P, P, P, P]
         lib.sd_pdraft_expand.restype = i32
+        lib.sd_pdraft_prepare.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32, i32,
+                                          P, P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P, i64,
+                                          P, P]
+        lib.sd_pdraft_prepare.restype = i32
         lib.sd_hidden_gather.argtypes = [i32, i32, P, P, P, i64, i32, P, P, i64, P, P]
         lib.sd_hidden_gather.restype = i32
         lib.sd_philox_words.argtypes = [i32, P, u64, P, P]
@@ -141,6 +145,25 @@ def sd_pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, ma
         _ptr(is_rejected), _ptr(start_loc), _ptr(new_token_idx), _ptr(total_out), _ptr(err),
         _stream(start_loc, stream))
     _check(rc, "sd_pdraft_expand")
+
+
+def sd_pdraft_prepare(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,
+                      input_ids, positions, slot_mapping, hidden_map, is_masked, is_rejected,
+                      start_loc, new_token_idx, total_out, target_hidden, h_shared, out_hidden,
+                      err=None, stream=None):
+    """sd_pdraft_expand and the hidden-state gather in one launch (see include/sd.h)."""
+    B, K1 = out_tokens.shape
+    cap, H = out_hidden.shape
+    if input_ids.shape[0] != cap:
+        raise SDError("out_hidden must have one row per drafter slot")
+    rc = load().sd_pdraft_prepare(
+        B, K1 - 1, _ptr(out_tokens), _ptr(num_accepted), _ptr(pos0), _ptr(block_table),
+        block_table.shape[1], block_size, mask_token_id, cap, _ptr(input_ids), _ptr(positions),
+        _ptr(slot_mapping), _ptr(hidden_map), _ptr(is_masked), _ptr(is_rejected),
+        _ptr(start_loc), _ptr(new_token_idx), _ptr(total_out), H, _ptr(target_hidden),
+        _row_stride(target_hidden), target_hidden.shape[0], _ptr(h_shared), _ptr(out_hidden),
+        _row_stride(out_hidden), _ptr(err), _stream(start_loc, stream))
+    _check(rc, "sd_pdraft_prepare")
 
 
 def sd_hidden_gather(total_out, hidden_map, target_hidden, h_shared, out_hidden, err=None,

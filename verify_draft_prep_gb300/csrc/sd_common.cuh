@@ -63,15 +63,14 @@ __device__ __forceinline__ float race_E_exact(uint32_t w) {
   return __double2float_rn(-log(v));
 }
 
-// Fast filter value for the race: Ls ~= -log2(v) * 2^64, from one hardware lg2 on an fp32 v.
-// Near v = 1 (the top 2^-8 of the w range) -log(v) is formed from m = 1 - v by its series,
-// because the fp32 rounding of v would cost too many relative bits there. The factor 2^64
-// keeps every product of a residual with Ls in the normal range. Its worst relative error
-// against the exact E (times log2(e) * 2^64) over all 2^32 words is checked exhaustively by
-// sd_race_E_approx_error; the race filter's bands are 16x wider.
-constexpr float kTwo64 = 18446744073709551616.0f;
+// Fast filter value for the race: R ~= 2^64 / (-log2 v), proportional to 1/E, from one hardware
+// lg2 and one hardware reciprocal on an fp32 v. Within 2^-13 of v = 1 (w >= kNearOne, one word
+// in 8192) the hardware lg2 loses relative accuracy, so there -log2(v) is formed from m = 1 - v
+// by its series instead. The scale 2^64 keeps r * R in the normal range for every positive fp32
+// residual r <= 2^30. The worst relative error of R against 2^64 / (E * log2(e)) over all 2^32
+// words is measured exhaustively by sd_race_E_approx_error; the race filter's band is 8x wider.
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kNearOne = 0xFF000000u;  // w >= this: v > 1 - 2^-8
+constexpr uint32_t kNearOne = 0xFFF80000u;  // w >= this: 1 - v < 2^-13
 
 __device__ __forceinline__ float fast_lg2(float x) {
   float y;
@@ -79,18 +78,25 @@ __device__ __forceinline__ float fast_lg2(float x) {
   return y;
 }
 
-__device__ __forceinline__ float race_Ls(uint32_t w) {
-  float Ls;
-  if (w < kNearOne) {
-    const float v = fmaf(__uint2float_rn(w), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
-    Ls = fast_lg2(v) * (-kTwo64);
-  } else {
-    const float m = fmaf(__uint2float_rn(~w), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
-    // -ln(1 - m) = m + m^2/2 + m^3/3 + m^4/4 + ...; for m < 2^-8 the tail is below 2^-26 m.
-    const float s = fmaf(m, fmaf(m, fmaf(m, 0.25f, 0.33333334f), 0.5f), 1.0f);
-    Ls = (m * s) * (kLog2e * kTwo64);
-  }
-  return Ls;
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float race_R_main(uint32_t w) {
+  const float v = fmaf(__uint2float_rn(w), 0x1p-32f, 0x1p-33f);
+  return fast_rcp(fast_lg2(v) * -0x1p-64f);
+}
+
+__device__ __forceinline__ float race_R_near_one(uint32_t w) {
+  const float m = fmaf(__uint2float_rn(~w), 0x1p-32f, 0x1p-33f);  // 1 - v, m < 2^-13
+  // -ln(1 - m) = m (1 + m/2 + m^2/3 + ...); the dropped terms are below 2^-27 relative.
+  return fast_rcp((m * fmaf(m, 0.5f, 1.0f)) * (kLog2e * 0x1p-64f));
+}
+
+__device__ __forceinline__ float race_R(uint32_t w) {
+  return w < kNearOne ? race_R_main(w) : race_R_near_one(w);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -24,16 +24,14 @@ __global__ void race_E_kernel(int n, const uint32_t* w, float* E) {
   if (i < n) E[i] = race_E_exact(w[i]);
 }
 
-// max over w of |Ls(w) / (E(w) * log2(e) * 2^64) - 1|, evaluated in double.
+// max over w of |R(w) * E(w) * log2(e) / 2^64 - 1|, evaluated in double.
 __global__ void approx_error_kernel(uint32_t w_begin, unsigned long long count, float* max_rel) {
-  const double scale = 1.4426950408889634 * 18446744073709551616.0;
+  const double scale = 1.4426950408889634 / 18446744073709551616.0;
   double worst = 0.0;
   for (unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
        k < count; k += (unsigned long long)gridDim.x * blockDim.x) {
     const uint32_t w = (uint32_t)(w_begin + k);
-    const double approx = (double)race_Ls(w);
-    const double exact = (double)race_E_exact(w) * scale;
-    const double rel = fabs(approx / exact - 1.0);
+    const double rel = fabs((double)race_R(w) * (double)race_E_exact(w) * scale - 1.0);
     worst = rel > worst ? rel : worst;
   }
 #pragma unroll

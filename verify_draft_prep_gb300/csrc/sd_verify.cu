@@ -36,8 +36,7 @@ namespace sdk {
 constexpr int NT = 256;        // threads per CTA
 constexpr int UNROLL = 4;      // 16-byte units in flight per thread per row
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
-constexpr float kBandCand = 1.0f / 512.0f;  // candidate band (relative)
-constexpr float kBandDup = 1.0f / 256.0f;   // in-thread near-tie band (>= candidate band)
+constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
 
 struct VerifyParams {
   int B, K, V;
@@ -99,6 +98,7 @@ __device__ __forceinline__ float bf16_at(const uint4& w, int i) {
 template <bool HAS_Q>
 struct F32Residual {
   static constexpr int EPU = 4;
+  static constexpr int UNR = 4;  // units in flight per thread
   const float* p;
   const float* q;
   uint32_t V;
@@ -109,6 +109,10 @@ struct F32Residual {
   __device__ __forceinline__ void fetch(uint32_t u, Raw& raw) const {
     f32_unit(p, u, V, vec, 0.0f, raw.p);
     if (HAS_Q) f32_unit(q, u, V, vec, 0.0f, raw.q);
+  }
+  __device__ __forceinline__ void zero(Raw& raw) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw.p[i] = raw.q[i] = 0.0f;
   }
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[4]) const {
 #pragma unroll
@@ -128,6 +132,7 @@ __device__ __forceinline__ float logit_prob(float l, float M, float c, float inv
 template <bool HAS_Q>
 struct Bf16Residual {
   static constexpr int EPU = 8;
+  static constexpr int UNR = 2;
   const uint16_t* t;
   const uint16_t* d;
   float Mt, invSt, Md, invSd, c;
@@ -139,6 +144,9 @@ struct Bf16Residual {
   __device__ __forceinline__ void fetch(uint32_t u, Raw& raw) const {
     raw.t = bf16_raw(t, u, V, vec);
     if (HAS_Q) raw.d = bf16_raw(d, u, V, vec);
+  }
+  __device__ __forceinline__ void zero(Raw& raw) const {
+    raw.t = raw.d = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   }
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[8]) const {
 #pragma unroll
@@ -188,134 +196,123 @@ __device__ uint64_t cluster_max_u64(uint64_t v, Smem& sm, int& phase, int cl) {
 }
 
 // ------------------------------------------------------------------------------------ the race
-struct RaceState {
-  float rb, Lb;   // residual and scaled -log2 of the running best (its key is rb / Lb)
-  uint32_t xb;
-  bool dup;       // another element of this thread lies within kBandDup of the best
-};
-
-__device__ __forceinline__ void race_consider(RaceState& s, float r, float Ls, uint32_t x) {
-  if (r > 0.0f) {
-    const float c = r * s.Lb;  // compares r/Ls against rb/Lb without a division
-    const float d = s.rb * Ls;
-    if (c * (1.0f + kBandDup) >= d) {
-      if (c > d) {
-        s.dup = d * (1.0f + kBandDup) >= c;
-        s.rb = r;
-        s.Lb = Ls;
-        s.xb = x;
-      } else {
-        s.dup = true;
-      }
-    }
-  }
-}
+// Filter: the approximate key of element x is alpha_x = r(x) * R(w_x), proportional to r/E within
+// the measured relative error. Each thread keeps, branch-free, the largest unit maximum a1 (with
+// its unit) and the largest maximum among its other units a2. With A the CTA's largest a1, only
+// units whose maximum m satisfies m * (1 + kBand) >= A can hold the exact winner: the thread's
+// best unit if a1 qualifies, and any other of its units only if a2 does (then it rescans). Every
+// element of a candidate unit gets its exact key, so exact ties are settled by index.
 
 __device__ __forceinline__ uint64_t exact_key(float r, uint32_t w, uint32_t x) {
   const float key = __fdiv_rn(fmaxf(r, 0.0f), race_E_exact(w));
   return pack_key(__float_as_uint(key), x);
 }
 
-// Largest approximate key of the CTA, as a (residual, Ls) pair, broadcast to every thread.
-__device__ void block_best_pair(float rb, float Lb, float& rA, float& LA, Smem& sm) {
+// Largest approximate key of one unit (0 when no residual is positive).
+template <int EPU>
+__device__ __forceinline__ float unit_max_alpha(const float (&r)[EPU], const uint4 (&w)[EPU / 4]) {
+  float R[EPU];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ro = __shfl_xor_sync(0xffffffffu, rb, o);
-    const float Lo = __shfl_xor_sync(0xffffffffu, Lb, o);
-    if (ro * Lb > rb * Lo) {
-      rb = ro;
-      Lb = Lo;
+  for (int h = 0; h < EPU / 4; ++h) {
+    R[4 * h + 0] = race_R_main(w[h].x);
+    R[4 * h + 1] = race_R_main(w[h].y);
+    R[4 * h + 2] = race_R_main(w[h].z);
+    R[4 * h + 3] = race_R_main(w[h].w);
+  }
+  uint32_t wmax = 0;
+#pragma unroll
+  for (int h = 0; h < EPU / 4; ++h) wmax = max(wmax, max(max(w[h].x, w[h].y), max(w[h].z, w[h].w)));
+  if (wmax >= kNearOne) {  // one word in 8192: redo those few near v = 1
+#pragma unroll
+    for (int e = 0; e < EPU; ++e) {
+      const uint32_t we = word_of(w[e >> 2], e & 3);
+      if (we >= kNearOne) R[e] = race_R_near_one(we);
     }
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) {
-    sm.redf[0][warp] = rb;
-    sm.redf[1][warp] = Lb;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    rb = lane < NT / 32 ? sm.redf[0][lane] : 0.0f;
-    Lb = lane < NT / 32 ? sm.redf[1][lane] : 1.0f;
+  float m = 0.0f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ro = __shfl_xor_sync(0xffffffffu, rb, o);
-      const float Lo = __shfl_xor_sync(0xffffffffu, Lb, o);
-      if (ro * Lb > rb * Lo) {
-        rb = ro;
-        Lb = Lo;
-      }
-    }
-    if (lane == 0) sm.fbcast = make_float4(rb, Lb, 0.f, 0.f);
-  }
-  __syncthreads();
-  rA = sm.fbcast.x;
-  LA = sm.fbcast.y;
+  for (int e = 0; e < EPU; ++e) m = fmaxf(m, r[e] * R[e]);
+  return m;
 }
 
-// Exact race winner over units [u0, u1) of one row: returns the CTA's packed (key, ~x) maximum,
-// or 0 when no element of the chunk has a positive residual.
+template <class Src>
+__device__ __forceinline__ void unit_words(PhiloxKey key, uint32_t u, uint32_t rid, uint32_t j,
+                                           uint4 (&w)[Src::EPU / 4]) {
+#pragma unroll
+  for (int h = 0; h < Src::EPU / 4; ++h) w[h] = race_block(key, u * (Src::EPU / 4) + h, rid, j);
+}
+
+// Exact keys of the positive elements of unit u, folded into `best`.
+template <class Src>
+__device__ __noinline__ void exact_unit(const Src& src, uint32_t u, PhiloxKey key, uint32_t rid,
+                                           uint32_t j, uint64_t& best) {
+  constexpr int EPU = Src::EPU;
+  typename Src::Raw raw;
+  src.fetch(u, raw);
+  float r[EPU];
+  src.residual(raw, r);
+  uint4 w[EPU / 4];
+  unit_words<Src>(key, u, rid, j, w);
+#pragma unroll
+  for (int e = 0; e < EPU; ++e) {
+    if (r[e] > 0.0f) {
+      const uint64_t k = exact_key(r[e], word_of(w[e >> 2], e & 3), u * EPU + e);
+      best = k > best ? k : best;
+    }
+  }
+}
+
+// Exact race winner over units [u0, u1) of one row: the CTA's packed (key, ~x) maximum, or 0 when
+// no element of the chunk has a positive residual.
 template <class Src>
 __device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, PhiloxKey key,
                                uint32_t rid, uint32_t j, Smem& sm) {
   constexpr int EPU = Src::EPU;
-  RaceState s{0.0f, 1.0f, 0xffffffffu, false};
-  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * UNROLL) {
-    typename Src::Raw raw[UNROLL];
+  float a1 = 0.0f, a2 = 0.0f;
+  uint32_t best_u = 0xffffffffu;
+  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * Src::UNR) {
+    typename Src::Raw raw[Src::UNR];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
+    for (int k = 0; k < Src::UNR; ++k) {
       const uint32_t u = ub + k * NT;
       if (u < u1) src.fetch(u, raw[k]);
+      else src.zero(raw[k]);
     }
+    uint4 w[Src::UNR][EPU / 4];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const uint32_t u = ub + k * NT;
-      if (u < u1) {
-        float r[EPU];
-        src.residual(raw[k], r);
+    for (int k = 0; k < Src::UNR; ++k) unit_words<Src>(key, ub + k * NT, rid, j, w[k]);
 #pragma unroll
-        for (int h = 0; h < EPU / 4; ++h) {
-          const uint4 w = race_block(key, u * (EPU / 4) + h, rid, j);
-          const uint32_t x0 = u * EPU + 4 * h;
-          race_consider(s, r[4 * h + 0], race_Ls(w.x), x0 + 0);
-          race_consider(s, r[4 * h + 1], race_Ls(w.y), x0 + 1);
-          race_consider(s, r[4 * h + 2], race_Ls(w.z), x0 + 2);
-          race_consider(s, r[4 * h + 3], race_Ls(w.w), x0 + 3);
-        }
-      }
+    for (int k = 0; k < Src::UNR; ++k) {
+      float r[EPU];
+      src.residual(raw[k], r);
+      const float m = unit_max_alpha<EPU>(r, w[k]);
+      a2 = fmaxf(a2, fminf(m, a1));
+      best_u = m > a1 ? ub + k * NT : best_u;
+      a1 = fmaxf(a1, m);
     }
   }
-  float rA, LA;
-  block_best_pair(s.rb, s.Lb, rA, LA, sm);
+  const float A = __uint_as_float((uint32_t)block_max_u64<NT>(__float_as_uint(a1), sm.red));
   uint64_t best = 0ull;
-  if (rA > 0.0f) {
-    // A CTA maximum below about 2^-100 (subnormal territory for the keys): evaluate every
-    // positive element exactly, since fp32 rounding of tiny keys is no longer relative.
-    const bool tiny = !(rA * 0x1p100f >= LA * 0x1p-64f);
-    const bool cand = s.rb > 0.0f && (s.rb * LA * (1.0f + kBandCand) >= rA * s.Lb);
-    if (tiny || (cand && s.dup)) {
+  if (A > 0.0f) {
+    // A CTA maximum below about 2^-100 in key units: fp32 keys are near the subnormal range
+    // and no longer carry relative precision, so every positive element is evaluated exactly.
+    const bool tiny = A < 0x1p-37f;
+    if (tiny || a2 * (1.0f + kBand) >= A) {
       for (uint32_t u = u0 + threadIdx.x; u < u1; u += NT) {
-        typename Src::Raw raw;
-        src.fetch(u, raw);
-        float r[EPU];
-        src.residual(raw, r);
-#pragma unroll
-        for (int h = 0; h < EPU / 4; ++h) {
-          const uint4 w4 = race_block(key, u * (EPU / 4) + h, rid, j);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float rv = r[4 * h + i];
-            const uint32_t w = word_of(w4, i);
-            if (rv > 0.0f && (tiny || rv * LA * (1.0f + kBandCand) >= rA * race_Ls(w))) {
-              const uint64_t k = exact_key(rv, w, u * EPU + 4 * h + i);
-              best = k > best ? k : best;
-            }
-          }
+        bool take = tiny;
+        if (!take) {
+          typename Src::Raw raw;
+          src.fetch(u, raw);
+          float r[EPU];
+          src.residual(raw, r);
+          uint4 w[EPU / 4];
+          unit_words<Src>(key, u, rid, j, w);
+          take = unit_max_alpha<EPU>(r, w) * (1.0f + kBand) >= A;
         }
+        if (take) exact_unit(src, u, key, rid, j, best);
       }
-    } else if (cand) {
-      const uint4 w4 = race_block(key, s.xb >> 2, rid, j);
-      best = exact_key(src.at(s.xb), word_of(w4, s.xb & 3u), s.xb);
+    } else if (a1 * (1.0f + kBand) >= A) {
+      exact_unit(src, best_u, key, rid, j, best);
     }
   }
   return block_max_u64<NT>(best, sm.red);
@@ -690,6 +687,9 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
     }
   }
 
+  // Let a programmatically dependent launch (the draft-batch rebuild) get scheduled; it waits
+  // for this grid's completion before it reads any result.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
   if (crank == 0) {
     const int t = threadIdx.x;
