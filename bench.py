@@ -155,14 +155,16 @@ def alloc_outputs(w, device):
                 start_loc=torch.empty(B + 1, **i32), new_token_idx=torch.empty(B, K, **i32),
                 total_out=torch.empty(1, **i32),
                 out_hidden=torch.empty(cap, w.H, dtype=torch.bfloat16, device=device),
-                err=torch.zeros(1, **i32))
+                err=torch.zeros(1, **i32),
+                ws=torch.zeros(max(16, 16 * B), dtype=torch.uint8, device=device))
 
 
 def launch_step(sd, w, o, stream=None):
     """One step: verify, then the fused draft-batch rebuild + hidden gather (a programmatic
     dependent launch of verify)."""
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
-                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream)
+                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream,
+                 workspace_buf=o["ws"])
     sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
                          w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
                          o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
@@ -180,7 +182,8 @@ def launch_prepare(sd, w, o, stream=None):
 
 def launch_verify(sd, w, o, stream=None):
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
-                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream)
+                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream,
+                 workspace_buf=o["ws"])
 
 
 def time_graph(fn, sets, outs, stream, K):

@@ -101,12 +101,23 @@ extern "C" {
  *   p_at_draft, q_at_draft [B, K] fp32, each may be NULL: P and Q of every examined draft
  *     j <= min(a_r, K-1) (probabilities; raw target/draft values for T_r == 0; 0 for an
  *     out-of-range token), -1 for drafts never examined.
+ *   workspace, workspace_bytes: device scratch of at least sd_verify_workspace_bytes(B, K, V,
+ *     dtype) bytes, zeroed before first use and left zeroed by every call (see below).
  *   err: see above.
  */
-SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft,
-              long ld_d, const int32_t* drafts, const float* temperature, uint64_t seed,
-              int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
-              int32_t* err, void* stream);
+SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t,
+                     const void* draft, long ld_d, const int32_t* drafts,
+                     const float* temperature, uint64_t seed, int32_t* out_tokens,
+                     int32_t* num_accepted, float* p_at_draft, float* q_at_draft, void* workspace,
+                     size_t workspace_bytes, int32_t* err, void* stream);
+
+/*
+ * Size in bytes of the workspace sd_verify needs for B requests: 16 bytes per request, where the
+ * CTAs that share a request's race row merge their results. The caller allocates it (16-byte
+ * aligned) and zeroes it once; every sd_verify call leaves it zeroed again. Calls that may run
+ * concurrently need separate workspaces.
+ */
+SD_API size_t sd_verify_workspace_bytes(int B, int K, int V, int dtype);
 
 /*
  * sd_pdraft_expand -- rebuild of the drafter batch for P-EAGLE parallel drafting.

@@ -42,6 +42,36 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
   return c;
 }
 
+// The ten round keys precomputed on the host (k0 + i*W0, k1 + i*W1), kept in the kernel's
+// parameter space so that every round reads its key as a constant operand.
+struct PhiloxRoundKeys {
+  uint32_t k0[10], k1[10];
+};
+
+inline PhiloxRoundKeys philox_round_keys(uint64_t seed) {
+  PhiloxRoundKeys rk;
+  uint32_t k0 = (uint32_t)(seed & 0xffffffffu), k1 = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    rk.k0[i] = k0;
+    rk.k1[i] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return rk;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxRoundKeys& rk) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ rk.k0[i], lo1, hi0 ^ c.w ^ rk.k1[i], lo0);
+  }
+  return c;
+}
+
 __device__ __forceinline__ uint32_t word_of(uint4 v, uint32_t i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -56,6 +86,15 @@ __device__ __forceinline__ double accept_uniform(PhiloxKey key, uint32_t r, uint
 __device__ __forceinline__ uint4 race_block(PhiloxKey key, uint32_t g, uint32_t r, uint32_t j) {
   return philox4x32_10(make_uint4(g, j, r, 1u), key);
 }
+__device__ __forceinline__ uint4 race_block(const PhiloxRoundKeys& rk, uint32_t g, uint32_t r,
+                                            uint32_t j) {
+  return philox4x32_10(make_uint4(g, j, r, 1u), rk);
+}
+__device__ __forceinline__ double accept_uniform(const PhiloxRoundKeys& rk, uint32_t r,
+                                                 uint32_t j) {
+  const uint4 w = philox4x32_10(make_uint4(0u, j, r, 0u), rk);
+  return (double)(w.x >> 8) * (1.0 / 16777216.0);
+}
 
 // Exact race variate: E = fp32 rounding of the double -log(v), v = (w + 0.5) * 2^-32 (exact).
 __device__ __forceinline__ float race_E_exact(uint32_t w) {
@@ -64,23 +103,25 @@ __device__ __forceinline__ float race_E_exact(uint32_t w) {
 }
 
 // Fast filter value for the race: R ~= 2^64 / (-log2 v), proportional to 1/E, from one hardware
-// lg2 and one hardware reciprocal on an fp32 v. Within 2^-13 of v = 1 (w >= kNearOne, one word
-// in 8192) the hardware lg2 loses relative accuracy, so there -log2(v) is formed from m = 1 - v
+// lg2 and one hardware reciprocal on an fp32 v. Within 2^-11 of v = 1 (w >= kNearOne, one word
+// in 2048) the hardware lg2 loses relative accuracy, so there -log2(v) is formed from m = 1 - v
 // by its series instead. The scale 2^64 keeps r * R in the normal range for every positive fp32
 // residual r <= 2^30. The worst relative error of R against 2^64 / (E * log2(e)) over all 2^32
 // words is measured exhaustively by sd_race_E_approx_error; the race filter's band is 8x wider.
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kNearOne = 0xFFF80000u;  // w >= this: 1 - v < 2^-13
+constexpr uint32_t kNearOne = 0xFFE00000u;  // w >= this: 1 - v < 2^-11
 
+// The operands of these two are always normal numbers here (v >= 2^-33; -log2(v) * 2^-64 in
+// [2^-98, 2^-58]), so the flush-to-zero forms give the same results without subnormal handling.
 __device__ __forceinline__ float fast_lg2(float x) {
   float y;
-  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
 __device__ __forceinline__ float fast_rcp(float x) {
   float y;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -90,9 +131,9 @@ __device__ __forceinline__ float race_R_main(uint32_t w) {
 }
 
 __device__ __forceinline__ float race_R_near_one(uint32_t w) {
-  const float m = fmaf(__uint2float_rn(~w), 0x1p-32f, 0x1p-33f);  // 1 - v, m < 2^-13
-  // -ln(1 - m) = m (1 + m/2 + m^2/3 + ...); the dropped terms are below 2^-27 relative.
-  return fast_rcp((m * fmaf(m, 0.5f, 1.0f)) * (kLog2e * 0x1p-64f));
+  const float m = fmaf(__uint2float_rn(~w), 0x1p-32f, 0x1p-33f);  // 1 - v, m < 2^-11
+  // -ln(1 - m) = m (1 + m/2 + m^2/3 + ...); the dropped terms are below 2^-25 relative.
+  return fast_rcp((m * fmaf(m, fmaf(m, 0.33333334f, 0.5f), 1.0f)) * (kLog2e * 0x1p-64f));
 }
 
 __device__ __forceinline__ float race_R(uint32_t w) {

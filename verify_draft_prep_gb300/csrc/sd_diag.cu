@@ -47,20 +47,35 @@ __global__ void approx_error_kernel(uint32_t w_begin, unsigned long long count, 
 extern "C" int sd_philox_launch(int n, const uint32_t* ctr, uint64_t seed, uint32_t* out,
                                 cudaStream_t stream) {
   if (n == 0) return SD_OK;
-  sdk::philox_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, ctr, sdk::philox_key(seed), out);
-  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + 255) / 256), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, sdk::philox_kernel, n, ctr, sdk::philox_key(seed), out) ==
+                 cudaSuccess
+             ? SD_OK
+             : SD_E_LAUNCH;
 }
 
 extern "C" int sd_race_E_launch(int n, const uint32_t* w, float* E, cudaStream_t stream) {
   if (n == 0) return SD_OK;
-  sdk::race_E_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, w, E);
-  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + 255) / 256), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, sdk::race_E_kernel, n, w, E) == cudaSuccess ? SD_OK
+                                                                             : SD_E_LAUNCH;
 }
 
 extern "C" int sd_approx_error_launch(uint32_t w_begin, uint64_t count, float* max_rel,
                                       cudaStream_t stream) {
   if (count == 0) return SD_OK;
-  sdk::approx_error_kernel<<<152 * 8, 256, 0, stream>>>(w_begin, (unsigned long long)count,
-                                                         max_rel);
-  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(152 * 8, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, sdk::approx_error_kernel, w_begin,
+                            (unsigned long long)count, max_rel) == cudaSuccess
+             ? SD_OK
+             : SD_E_LAUNCH;
 }

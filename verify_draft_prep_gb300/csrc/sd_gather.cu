@@ -95,6 +95,9 @@ extern "C" int sd_gather_launch(int capacity, int H, const int32_t* total_out,
           ((uintptr_t)h_shared % 16 == 0) && ((uintptr_t)out_hidden % 16 == 0) &&
           (ld_in % 8 == 0) && (ld_out % 8 == 0);
   const int grid = capacity > 0 ? (capacity + sdk::GROWS - 1) / sdk::GROWS : 1;
-  sdk::gather_kernel<<<grid, sdk::GNT, 0, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(sdk::GNT, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, sdk::gather_kernel, P) == cudaSuccess ? SD_OK : SD_E_LAUNCH;
 }

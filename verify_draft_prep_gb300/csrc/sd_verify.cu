@@ -34,9 +34,18 @@
 namespace sdk {
 
 constexpr int NT = 256;        // threads per CTA
-constexpr int UNROLL = 4;      // 16-byte units in flight per thread per row
+constexpr int UNROLL = 4;      // 16-byte units in flight per thread (greedy rows, statistics)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
+constexpr int kCandCap = 32;            // candidate units evaluated lane-parallel per CTA
+
+// Per-request merge slot in the caller's workspace: the packed (key, ~x) maximum over the
+// request's CTAs and the number of CTAs that have merged. The last CTA resets both to zero.
+struct RaceSlot {
+  unsigned long long best;
+  unsigned int count;
+  unsigned int pad;
+};
 
 struct VerifyParams {
   int B, K, V;
@@ -46,11 +55,12 @@ struct VerifyParams {
   long ld_d;
   const int32_t* drafts;
   const float* temperature;
-  PhiloxKey key;
+  PhiloxRoundKeys rk;
   int32_t* out_tokens;
   int32_t* num_accepted;
   float* p_at;
   float* q_at;
+  struct RaceSlot* slots;  // one per request (sampled probability requests)
   int32_t* err;
   int cl;
   int vec;  // 1: every row starts on a 16-byte boundary
@@ -99,6 +109,7 @@ template <bool HAS_Q>
 struct F32Residual {
   static constexpr int EPU = 4;
   static constexpr int UNR = 4;  // units in flight per thread
+  static constexpr int ROWS = HAS_Q ? 2 : 1;
   const float* p;
   const float* q;
   uint32_t V;
@@ -113,6 +124,28 @@ struct F32Residual {
   __device__ __forceinline__ void zero(Raw& raw) const {
 #pragma unroll
     for (int i = 0; i < 4; ++i) raw.p[i] = raw.q[i] = 0.0f;
+  }
+  // units entirely inside the row, read with unchecked 128-bit loads when vec is set
+  __device__ __forceinline__ uint32_t full_units() const { return V / 4u; }
+  __device__ __forceinline__ const uint8_t* row_bytes(int r) const {
+    return (const uint8_t*)(r == 0 ? p : q);
+  }
+  __device__ __forceinline__ void from_smem(const uint8_t* const (&st)[ROWS], uint32_t i,
+                                            Raw& raw) const {
+    const float4 a = *reinterpret_cast<const float4*>(st[0] + 16u * i);
+    raw.p[0] = a.x; raw.p[1] = a.y; raw.p[2] = a.z; raw.p[3] = a.w;
+    if (HAS_Q) {
+      const float4 b = *reinterpret_cast<const float4*>(st[ROWS - 1] + 16u * i);
+      raw.q[0] = b.x; raw.q[1] = b.y; raw.q[2] = b.z; raw.q[3] = b.w;
+    }
+  }
+  __device__ __forceinline__ void fetch_fast(uint32_t u, Raw& raw) const {
+    const float4 a = ld_f4(p + 4u * u);
+    raw.p[0] = a.x; raw.p[1] = a.y; raw.p[2] = a.z; raw.p[3] = a.w;
+    if (HAS_Q) {
+      const float4 b = ld_f4(q + 4u * u);
+      raw.q[0] = b.x; raw.q[1] = b.y; raw.q[2] = b.z; raw.q[3] = b.w;
+    }
   }
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[4]) const {
 #pragma unroll
@@ -133,6 +166,7 @@ template <bool HAS_Q>
 struct Bf16Residual {
   static constexpr int EPU = 8;
   static constexpr int UNR = 2;
+  static constexpr int ROWS = HAS_Q ? 2 : 1;
   const uint16_t* t;
   const uint16_t* d;
   float Mt, invSt, Md, invSd, c;
@@ -147,6 +181,19 @@ struct Bf16Residual {
   }
   __device__ __forceinline__ void zero(Raw& raw) const {
     raw.t = raw.d = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  }
+  __device__ __forceinline__ uint32_t full_units() const { return V / 8u; }
+  __device__ __forceinline__ const uint8_t* row_bytes(int r) const {
+    return (const uint8_t*)(r == 0 ? t : d);
+  }
+  __device__ __forceinline__ void from_smem(const uint8_t* const (&st)[ROWS], uint32_t i,
+                                            Raw& raw) const {
+    raw.t = *reinterpret_cast<const uint4*>(st[0] + 16u * i);
+    if (HAS_Q) raw.d = *reinterpret_cast<const uint4*>(st[ROWS - 1] + 16u * i);
+  }
+  __device__ __forceinline__ void fetch_fast(uint32_t u, Raw& raw) const {
+    raw.t = ld_stream_u4(t + 8u * u);
+    if (HAS_Q) raw.d = ld_stream_u4(d + 8u * u);
   }
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[8]) const {
 #pragma unroll
@@ -172,6 +219,9 @@ struct Smem {
   float P[SD_K_MAX], Q[SD_K_MAX];
   int a;
   int e;
+  int ncand;
+  uint32_t cand[kCandCap];
+  int last;
 };
 
 // Cluster-wide maximum of a CTA-uniform value. Every CTA of the cluster calls it the same
@@ -236,23 +286,23 @@ __device__ __forceinline__ float unit_max_alpha(const float (&r)[EPU], const uin
 }
 
 template <class Src>
-__device__ __forceinline__ void unit_words(PhiloxKey key, uint32_t u, uint32_t rid, uint32_t j,
-                                           uint4 (&w)[Src::EPU / 4]) {
+__device__ __forceinline__ void unit_words(const PhiloxRoundKeys& rk, uint32_t u, uint32_t rid,
+                                           uint32_t j, uint4 (&w)[Src::EPU / 4]) {
 #pragma unroll
-  for (int h = 0; h < Src::EPU / 4; ++h) w[h] = race_block(key, u * (Src::EPU / 4) + h, rid, j);
+  for (int h = 0; h < Src::EPU / 4; ++h) w[h] = race_block(rk, u * (Src::EPU / 4) + h, rid, j);
 }
 
-// Exact keys of the positive elements of unit u, folded into `best`.
+// Exact keys of the positive elements of unit u, folded into `best` (one thread, rare path).
 template <class Src>
-__device__ __noinline__ void exact_unit(const Src& src, uint32_t u, PhiloxKey key, uint32_t rid,
-                                           uint32_t j, uint64_t& best) {
+__device__ __noinline__ void exact_unit(const Src& src, uint32_t u, const PhiloxRoundKeys& rk,
+                                        uint32_t rid, uint32_t j, uint64_t& best) {
   constexpr int EPU = Src::EPU;
   typename Src::Raw raw;
   src.fetch(u, raw);
   float r[EPU];
   src.residual(raw, r);
   uint4 w[EPU / 4];
-  unit_words<Src>(key, u, rid, j, w);
+  unit_words<Src>(rk, u, rid, j, w);
 #pragma unroll
   for (int e = 0; e < EPU; ++e) {
     if (r[e] > 0.0f) {
@@ -262,42 +312,60 @@ __device__ __noinline__ void exact_unit(const Src& src, uint32_t u, PhiloxKey ke
   }
 }
 
+template <class Src>
+__device__ __forceinline__ void race_take(const Src& src, const typename Src::Raw& raw,
+                                          const uint4 (&w)[Src::EPU / 4], uint32_t u, float& a1,
+                                          float& a2, uint32_t& best_u) {
+  float r[Src::EPU];
+  src.residual(raw, r);
+  const float m = unit_max_alpha<Src::EPU>(r, w);
+  a2 = fmaxf(a2, fminf(m, a1));
+  best_u = m > a1 ? u : best_u;
+  a1 = fmaxf(a1, m);
+}
+
 // Exact race winner over units [u0, u1) of one row: the CTA's packed (key, ~x) maximum, or 0 when
 // no element of the chunk has a positive residual.
 template <class Src>
-__device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, PhiloxKey key,
+__device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, const PhiloxRoundKeys& rk,
                                uint32_t rid, uint32_t j, Smem& sm) {
-  constexpr int EPU = Src::EPU;
+  constexpr int EPU = Src::EPU, UNR = Src::UNR;
   float a1 = 0.0f, a2 = 0.0f;
   uint32_t best_u = 0xffffffffu;
-  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * Src::UNR) {
-    typename Src::Raw raw[Src::UNR];
+  // units [u0, uf) lie inside 16-byte aligned rows: unchecked 128-bit loads, UNR units in flight
+  const uint32_t uf = src.vec ? max(u0, min(u1, src.full_units())) : u0;
+  uint32_t ub = u0 + threadIdx.x;
+  for (; ub + (UNR - 1) * NT < uf; ub += NT * UNR) {
+    typename Src::Raw raw[UNR];
 #pragma unroll
-    for (int k = 0; k < Src::UNR; ++k) {
-      const uint32_t u = ub + k * NT;
-      if (u < u1) src.fetch(u, raw[k]);
-      else src.zero(raw[k]);
-    }
-    uint4 w[Src::UNR][EPU / 4];
+    for (int k = 0; k < UNR; ++k) src.fetch_fast(ub + k * NT, raw[k]);
+    uint4 w[UNR][EPU / 4];
 #pragma unroll
-    for (int k = 0; k < Src::UNR; ++k) unit_words<Src>(key, ub + k * NT, rid, j, w[k]);
+    for (int k = 0; k < UNR; ++k) unit_words<Src>(rk, ub + k * NT, rid, j, w[k]);
 #pragma unroll
-    for (int k = 0; k < Src::UNR; ++k) {
-      float r[EPU];
-      src.residual(raw[k], r);
-      const float m = unit_max_alpha<EPU>(r, w[k]);
-      a2 = fmaxf(a2, fminf(m, a1));
-      best_u = m > a1 ? ub + k * NT : best_u;
-      a1 = fmaxf(a1, m);
-    }
+    for (int k = 0; k < UNR; ++k) race_take(src, raw[k], w[k], ub + k * NT, a1, a2, best_u);
   }
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked
+    typename Src::Raw raw;
+    src.fetch(ub, raw);
+    uint4 w[EPU / 4];
+    unit_words<Src>(rk, ub, rid, j, w);
+    race_take(src, raw, w, ub, a1, a2, best_u);
+  }
+  if (threadIdx.x == 0) sm.ncand = 0;
   const float A = __uint_as_float((uint32_t)block_max_u64<NT>(__float_as_uint(a1), sm.red));
   uint64_t best = 0ull;
   if (A > 0.0f) {
     // A CTA maximum below about 2^-100 in key units: fp32 keys are near the subnormal range
     // and no longer carry relative precision, so every positive element is evaluated exactly.
     const bool tiny = A < 0x1p-37f;
-    if (tiny || a2 * (1.0f + kBand) >= A) {
+    bool rescan = tiny || a2 * (1.0f + kBand) >= A;
+    if (!rescan && a1 * (1.0f + kBand) >= A) {
+      const int slot = atomicAdd(&sm.ncand, 1);
+      if (slot < kCandCap) sm.cand[slot] = best_u;
+      else rescan = true;
+    }
+    if (rescan) {  // this thread's other units may hold candidates too (rare)
       for (uint32_t u = u0 + threadIdx.x; u < u1; u += NT) {
         bool take = tiny;
         if (!take) {
@@ -306,13 +374,29 @@ __device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, PhiloxK
           float r[EPU];
           src.residual(raw, r);
           uint4 w[EPU / 4];
-          unit_words<Src>(key, u, rid, j, w);
+          unit_words<Src>(rk, u, rid, j, w);
           take = unit_max_alpha<EPU>(r, w) * (1.0f + kBand) >= A;
         }
-        if (take) exact_unit(src, u, key, rid, j, best);
+        if (take) exact_unit(src, u, rk, rid, j, best);
       }
-    } else if (a1 * (1.0f + kBand) >= A) {
-      exact_unit(src, best_u, key, rid, j, best);
+    }
+    __syncthreads();
+    // the listed candidate units, one element per lane
+    const int nc = min(sm.ncand, kCandCap);
+    if (threadIdx.x < 32) {
+      for (int base = 0; base < nc * EPU; base += 32) {
+        const int l = base + (int)threadIdx.x;
+        if (l < nc * EPU) {
+          const uint32_t u = sm.cand[l / EPU];
+          const uint32_t x = u * EPU + (uint32_t)(l % EPU);
+          const float r = x < src.V ? src.at(x) : 0.0f;  // the last unit may pass the row end
+          if (r > 0.0f) {
+            const uint4 w4 = race_block(rk, x >> 2, rid, j);
+            const uint64_t k = exact_key(r, word_of(w4, x & 3u), x);
+            best = k > best ? k : best;
+          }
+        }
+      }
     }
   }
   return block_max_u64<NT>(best, sm.red);
@@ -329,39 +413,40 @@ __device__ __forceinline__ void argmax_take(float v, uint32_t x, float& best, ui
 template <int DT>
 __device__ uint64_t argmax_chunk(const void* row, uint32_t V, bool vec, uint32_t u0, uint32_t u1,
                                  Smem& sm) {
+  constexpr int EPU = DT == SD_F32_PROBS ? 4 : 8;
   float best = -INFINITY;
   uint32_t bx = 0xffffffffu;
-  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * UNROLL) {
+  const uint32_t uf = vec ? max(u0, min(u1, V / EPU)) : u0;
+  uint32_t ub = u0 + threadIdx.x;
+  for (; ub + (UNROLL - 1) * NT < uf; ub += NT * UNROLL) {  // unchecked 128-bit loads
+    uint4 v[UNROLL];
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k)
+      v[k] = ld_stream_u4((const char*)row + (size_t)(ub + k * NT) * 16u);
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) {
+      const uint32_t x0 = (ub + k * NT) * EPU;
+      if (DT == SD_F32_PROBS) {
+        argmax_take(__uint_as_float(v[k].x), x0 + 0, best, bx);
+        argmax_take(__uint_as_float(v[k].y), x0 + 1, best, bx);
+        argmax_take(__uint_as_float(v[k].z), x0 + 2, best, bx);
+        argmax_take(__uint_as_float(v[k].w), x0 + 3, best, bx);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v[k], i), x0 + i, best, bx);
+      }
+    }
+  }
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked
     if (DT == SD_F32_PROBS) {
-      float v[UNROLL][4];
+      float v[4];
+      f32_unit((const float*)row, ub, V, vec, -INFINITY, v);
 #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const uint32_t u = ub + k * NT;
-        if (u < u1) f32_unit((const float*)row, u, V, vec, -INFINITY, v[k]);
-      }
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const uint32_t u = ub + k * NT;
-        if (u < u1) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) argmax_take(v[k][i], u * 4 + i, best, bx);
-        }
-      }
+      for (int i = 0; i < 4; ++i) argmax_take(v[i], ub * 4 + i, best, bx);
     } else {
-      uint4 v[UNROLL];
+      const uint4 v = bf16_raw((const uint16_t*)row, ub, V, vec);
 #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const uint32_t u = ub + k * NT;
-        if (u < u1) v[k] = bf16_raw((const uint16_t*)row, u, V, vec);
-      }
-#pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
-        const uint32_t u = ub + k * NT;
-        if (u < u1) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v[k], i), u * 8 + i, best, bx);
-        }
-      }
+      for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v, i), ub * 8 + i, best, bx);
     }
   }
   const uint64_t pk = (bx == 0xffffffffu) ? 0ull : pack_key(orderable(best), bx);
@@ -449,24 +534,24 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
                           int& phase, int cl) {
   MaxSum a{-INFINITY, 0.0f}, b{-INFINITY, 0.0f};
   float ca = 0.0f, cb = 0.0f;
-  for (uint32_t ub = u0 + threadIdx.x; ub < u1; ub += NT * UNROLL) {
+  const uint32_t uf = vec ? max(u0, min(u1, V / 8u)) : u0;
+  uint32_t ub = u0 + threadIdx.x;
+  for (; ub + (UNROLL - 1) * NT < uf; ub += NT * UNROLL) {  // unchecked 128-bit loads
     uint4 vt[UNROLL], vd[UNROLL];
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
-      const uint32_t u = ub + k * NT;
-      if (u < u1) {
-        vt[k] = bf16_raw(trow, u, V, vec);
-        if (HAS_Q) vd[k] = bf16_raw(drow, u, V, vec);
-      }
+      vt[k] = ld_stream_u4(trow + 8u * (ub + k * NT));
+      if (HAS_Q) vd[k] = ld_stream_u4(drow + 8u * (ub + k * NT));
     }
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
-      const uint32_t u = ub + k * NT;
-      if (u < u1) {
-        absorb_unit(a, ca, vt[k], c);
-        if (HAS_Q) absorb_unit(b, cb, vd[k], c);
-      }
+      absorb_unit(a, ca, vt[k], c);
+      if (HAS_Q) absorb_unit(b, cb, vd[k], c);
     }
+  }
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked
+    absorb_unit(a, ca, bf16_raw(trow, ub, V, vec), c);
+    if (HAS_Q) absorb_unit(b, cb, bf16_raw(drow, ub, V, vec), c);
   }
   a.s -= ca;
   b.s -= cb;
@@ -494,7 +579,7 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
 
 // ---------------------------------------------------------------------------------- the kernel
 template <int DT>
-__global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ VerifyParams P) {
   __shared__ Smem sm;
   constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
   using Elt = typename std::conditional<DT == SD_F32_PROBS, float, uint16_t>::type;
@@ -518,6 +603,8 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
   int a = K;
   uint32_t b = 0;
   int32_t e = 0;
+  bool writer = crank == 0;  // the CTA that writes the request's outputs
+  const bool sampled_probs = DT == SD_F32_PROBS && !greedy;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x < SD_K_MAX) {
@@ -571,7 +658,7 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
         if (d >= 0 && (uint32_t)d < V) {
           Pv = __ldg((const float*)trow(j) + d);
           Qv = __ldg((const float*)drow(j) + d);
-          const double u = accept_uniform(P.key, (uint32_t)r, (uint32_t)j);
+          const double u = accept_uniform(P.rk, (uint32_t)r, (uint32_t)j);
           acc = u * (double)Qv < (double)Pv;  // u*Q is exact in double
         } else {
           bad = true;
@@ -596,21 +683,44 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
     uint64_t pk;
     if (a < K) {
       F32Residual<true> src{(const float*)trow(jr), (const float*)drow(jr), V, vec};
-      pk = cluster_max_u64(race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)jr, sm), sm,
-                           phase, cl);
+      pk = race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm);
     } else {
-      pk = 0ull;
-    }
-    if (packed_key_bits(pk) == 0u) {  // bonus race, or no positive residual key: race on p
       F32Residual<false> src{(const float*)trow(jr), nullptr, V, vec};
-      pk = cluster_max_u64(race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)jr, sm), sm,
-                           phase, cl);
+      pk = race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm);
     }
-    if (packed_key_bits(pk) == 0u) {
-      e |= SD_ERR_ZERO_ROW;
-      b = 0;
-    } else {
-      b = packed_index(pk);
+    // Merge into the request's slot; the CTA that merges last finishes the request. No CTA
+    // waits for another.
+    RaceSlot* slot = P.slots + r;
+    if (threadIdx.x == 0) {
+      if (pk) atomicMax(&slot->best, (unsigned long long)pk);
+      __threadfence();
+      const unsigned prev = atomicAdd(&slot->count, 1u);
+      sm.last = (prev == (unsigned)cl - 1u);
+    }
+    __syncthreads();
+    writer = sm.last != 0;
+    if (writer) {
+      if (threadIdx.x == 0) {
+        __threadfence();
+        sm.bcast = atomicOr(&slot->best, 0ull);  // every other CTA's maximum is in by now
+      }
+      __syncthreads();
+      pk = sm.bcast;
+      if (packed_key_bits(pk) == 0u && a < K) {
+        // no positive residual key anywhere in the row: race on p of the same row, whole row
+        F32Residual<false> src{(const float*)trow(jr), nullptr, V, vec};
+        pk = race_chunk(src, 0u, NU, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+      }
+      if (packed_key_bits(pk) == 0u) {
+        e |= SD_ERR_ZERO_ROW;
+        b = 0;
+      } else {
+        b = packed_index(pk);
+      }
+      if (threadIdx.x == 0) {
+        slot->best = 0ull;
+        slot->count = 0u;
+      }
     }
   } else {
     // ---- sampled, bf16 logit rows: per row max/sum, decide, race on the rejected row
@@ -638,7 +748,7 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
                                                   sd.m),
                                         c)),
                        sd.s);
-        const double u = accept_uniform(P.key, (uint32_t)r, (uint32_t)j);
+        const double u = accept_uniform(P.rk, (uint32_t)r, (uint32_t)j);
         accept = u * (double)Qv < (double)Pv;
       } else {
         e |= SD_ERR_TOKEN_RANGE;
@@ -653,11 +763,11 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
         Bf16Residual<true> src{t16 + (size_t)j * P.ld_t, d16 + (size_t)j * P.ld_d, st.m,
                                1.0f / st.s, sd.m, 1.0f / sd.s, c, V, vec};
         uint64_t pk = cluster_max_u64(
-            race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)j, sm), sm, phase, cl);
+            race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)j, sm), sm, phase, cl);
         if (packed_key_bits(pk) == 0u) {
           Bf16Residual<false> srcp{t16 + (size_t)j * P.ld_t, nullptr, st.m, 1.0f / st.s,
                                    0.0f, 0.0f, c, V, vec};
-          pk = cluster_max_u64(race_chunk(srcp, u0, u1, P.key, (uint32_t)r, (uint32_t)j, sm),
+          pk = cluster_max_u64(race_chunk(srcp, u0, u1, P.rk, (uint32_t)r, (uint32_t)j, sm),
                                sm, phase, cl);
         }
         if (packed_key_bits(pk) == 0u) {
@@ -677,7 +787,7 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
       Bf16Residual<false> src{t16 + (size_t)jr * P.ld_t, nullptr, st.m, 1.0f / st.s,
                               0.0f, 0.0f, c, V, vec};
       const uint64_t pk = cluster_max_u64(
-          race_chunk(src, u0, u1, P.key, (uint32_t)r, (uint32_t)jr, sm), sm, phase, cl);
+          race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm), sm, phase, cl);
       if (packed_key_bits(pk) == 0u) {
         e |= SD_ERR_ZERO_ROW;
         b = 0;
@@ -691,7 +801,7 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
   // for this grid's completion before it reads any result.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
-  if (crank == 0) {
+  if (writer) {
     const int t = threadIdx.x;
     if (t <= K) {
       int32_t tok = -1;
@@ -708,12 +818,20 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const VerifyParams P) {
       raise_err(P.err, e);
     }
   }
-  if (cl > 1) cluster_barrier();  // peers may still read this CTA's shared memory
+  // greedy and logit requests exchanged data through distributed shared memory: peers may still
+  // read this CTA's shared memory until all have passed this barrier
+  if (cl > 1 && !sampled_probs) cluster_barrier();
 }
 
 }  // namespace sdk
 
 // ------------------------------------------------------------------------------------ launcher
+namespace {
+
+}  // namespace
+
+extern "C" size_t sd_verify_workspace_launch(int B) { return (size_t)B * sizeof(sdk::RaceSlot); }
+
 namespace {
 
 int choose_cluster(int V, int epu) {
@@ -729,7 +847,7 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
                                 const void* draft, long ld_d, const int32_t* drafts,
                                 const float* temperature, uint64_t seed, int32_t* out_tokens,
                                 int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
-                                int32_t* err, cudaStream_t stream) {
+                                void* workspace, int32_t* err, cudaStream_t stream) {
   const int esize = dtype == SD_F32_PROBS ? 4 : 2;
   const int epu = dtype == SD_F32_PROBS ? 4 : 8;
   sdk::VerifyParams P;
@@ -742,11 +860,12 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.ld_d = ld_d;
   P.drafts = drafts;
   P.temperature = temperature;
-  P.key = sdk::philox_key(seed);
+  P.rk = sdk::philox_round_keys(seed);
   P.out_tokens = out_tokens;
   P.num_accepted = num_accepted;
   P.p_at = p_at_draft;
   P.q_at = q_at_draft;
+  P.slots = (sdk::RaceSlot*)workspace;
   P.err = err;
   P.cl = choose_cluster(V, epu);
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
