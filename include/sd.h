@@ -50,6 +50,7 @@ extern "C" {
 #define SD_E_ALIGN (-4)    /* a pointer or stride breaks the stated alignment */
 #define SD_E_LAUNCH (-5)   /* the CUDA launch failed (cudaGetLastError is left set) */
 #define SD_E_DEVICE (-6)   /* no usable sm_103 device is current */
+#define SD_E_NOALLOC_LIMIT (-7) /* B > SD_VERIFY_NOALLOC_MAX_B for sd_verify_noalloc */
 
 /* device-side data error bits, OR-ed into *err */
 #define SD_ERR_TOKEN_RANGE 1    /* a draft token outside [0, V): treated as rejected */
@@ -118,6 +119,29 @@ SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld
  * concurrently need separate workspaces.
  */
 SD_API size_t sd_verify_workspace_bytes(int B, int K, int V, int dtype);
+
+/*
+ * sd_verify_noalloc -- sd_verify for callers that cannot allocate device memory. This call has
+ * no counterpart in the method's sources; it exists for callers such as a plugin or engine
+ * that is handed only its input and output buffers and may not call cudaMalloc (allocation
+ * would stall or break the host runtime's memory pool, or happen inside a stream capture that
+ * forbids it). Same arguments, semantics and results as sd_verify, minus the workspace: the
+ * merge slots live in a fixed device array of SD_VERIFY_NOALLOC_MAX_B entries (16 bytes each)
+ * that every GPU loading the library holds until the process exits.
+ *   - B > SD_VERIFY_NOALLOC_MAX_B returns SD_E_NOALLOC_LIMIT and enqueues nothing.
+ *   - The first call on a device looks the array's address up (cudaGetSymbolAddress) with that
+ *     device current; make that first call before any stream capture.
+ *   - Each call enqueues a clear of the slots it uses and then the verify kernel; it calls no
+ *     allocator.
+ *   - All calls on a device share the one array: calls that may overlap on the GPU (other
+ *     streams, other host threads) race on it and must be serialised by the caller.
+ */
+#define SD_VERIFY_NOALLOC_MAX_B 4096
+SD_API int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target, long ld_t,
+                             const void* draft, long ld_d, const int32_t* drafts,
+                             const float* temperature, uint64_t seed, int32_t* out_tokens,
+                             int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+                             int32_t* err, void* stream);
 
 /*
  * sd_pdraft_expand -- rebuild of the drafter batch for P-EAGLE parallel drafting.

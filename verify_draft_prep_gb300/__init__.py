@@ -20,6 +20,7 @@ from ._build import build
 SD_F32_PROBS = 0
 SD_BF16_LOGITS = 1
 SD_K_MAX = 16
+SD_VERIFY_NOALLOC_MAX_B = 4096
 
 SD_ERR_TOKEN_RANGE = 1
 SD_ERR_BLOCK_TABLE = 2
@@ -28,7 +29,7 @@ SD_ERR_MAP_RANGE = 8
 SD_ERR_ZERO_ROW = 16
 SD_ERR_TOTAL_RANGE = 32
 
-EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_noalloc", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -53,6 +54,9 @@ def load():
         lib.sd_verify.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, P, P, P, P, P,
                                   ctypes.c_size_t, P, P]
         lib.sd_verify.restype = i32
+        lib.sd_verify_noalloc.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, P, P,
+                                          P, P, P, P]
+        lib.sd_verify_noalloc.restype = i32
         lib.sd_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.sd_verify_workspace_bytes.restype = ctypes.c_size_t
         lib.sd_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32, i32,

@@ -11,6 +11,9 @@ int sd_verify_launch(int, int, int, int, const void*, long, const void*, long, c
                      const float*, uint64_t, int32_t*, int32_t*, float*, float*, void*, int32_t*,
                      cudaStream_t);
 size_t sd_verify_workspace_launch(int);
+int sd_verify_noalloc_launch(int, int, int, int, const void*, long, const void*, long,
+                             const int32_t*, const float*, uint64_t, int32_t*, int32_t*, float*,
+                             float*, int32_t*, cudaStream_t);
 int sd_prep_launch(int, int, const int32_t*, const int32_t*, const int32_t*, const int32_t*, int,
                    int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
                    int32_t*, int32_t*, int32_t*, int, const void*, long, int, const void*, void*,
@@ -56,6 +59,8 @@ const char* sd_status_string(int status) {
     case SD_E_ALIGN: return "a pointer or stride breaks the required alignment";
     case SD_E_LAUNCH: return "CUDA launch failed";
     case SD_E_DEVICE: return "the current device is not an sm_103 GPU";
+    case SD_E_NOALLOC_LIMIT:
+      return "B exceeds the fixed scratch of sd_verify_noalloc (SD_VERIFY_NOALLOC_MAX_B requests)";
     default: return "unknown status";
   }
 }
@@ -85,6 +90,25 @@ int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, con
   return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
                           out_tokens, num_accepted, p_at_draft, q_at_draft, workspace, err,
                           (cudaStream_t)stream);
+}
+
+int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target, long ld_t,
+                      const void* draft, long ld_d, const int32_t* drafts,
+                      const float* temperature, uint64_t seed, int32_t* out_tokens,
+                      int32_t* num_accepted, float* p_at_draft, float* q_at_draft, int32_t* err,
+                      void* stream) {
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
+  if (B > SD_VERIFY_NOALLOC_MAX_B) return SD_E_NOALLOC_LIMIT;
+  if (B == 0) return SD_OK;
+  if (!target || !draft || !drafts || !out_tokens || !num_accepted) return SD_E_NULL;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  if ((uintptr_t)target % esize || (uintptr_t)draft % esize) return SD_E_ALIGN;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_verify_noalloc_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature,
+                                  seed, out_tokens, num_accepted, p_at_draft, q_at_draft, err,
+                                  (cudaStream_t)stream);
 }
 
 namespace {

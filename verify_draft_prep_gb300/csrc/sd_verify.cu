@@ -27,6 +27,7 @@
 #include <float.h>
 #include <math.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "sd_common.cuh"
@@ -888,4 +889,40 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   if (dtype == SD_F32_PROBS) rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_F32_PROBS>, P);
   else rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_BF16_LOGITS>, P);
   return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}
+
+// ------------------------------------------------------------------ no-allocation entry point
+// Scratch for sd_verify_noalloc: the same per-request merge slots sd_verify keeps in the caller's
+// workspace, here in a fixed array that every GPU loading the library holds until exit
+// (SD_VERIFY_NOALLOC_MAX_B * 16 bytes). Host code may not pass the array's name to a kernel (on
+// the host it is only a stand-in for the device symbol); its device address is looked up once
+// per device, with that device current.
+static __device__ __align__(256) sdk::RaceSlot g_noalloc_slots[SD_VERIFY_NOALLOC_MAX_B];
+
+namespace {
+constexpr int kNoallocMaxDevices = 64;
+std::atomic<void*> g_noalloc_addr[kNoallocMaxDevices];
+}  // namespace
+
+extern "C" int sd_verify_noalloc_launch(int B, int K, int V, int dtype, const void* target,
+                                        long ld_t, const void* draft, long ld_d,
+                                        const int32_t* drafts, const float* temperature,
+                                        uint64_t seed, int32_t* out_tokens, int32_t* num_accepted,
+                                        float* p_at_draft, float* q_at_draft, int32_t* err,
+                                        cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices)
+    return SD_E_DEVICE;
+  void* slots = g_noalloc_addr[dev].load();
+  if (!slots) {
+    if (cudaGetSymbolAddress(&slots, g_noalloc_slots) != cudaSuccess || !slots)
+      return SD_E_LAUNCH;
+    g_noalloc_addr[dev].store(slots);
+  }
+  // The slots must start at zero; every call leaves them zeroed, but clear them anyway so that
+  // no earlier call's state can leak into this one.
+  if (cudaMemsetAsync(slots, 0, (size_t)B * sizeof(sdk::RaceSlot), stream) != cudaSuccess)
+    return SD_E_LAUNCH;
+  return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
+                          out_tokens, num_accepted, p_at_draft, q_at_draft, slots, err, stream);
 }
