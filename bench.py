@@ -264,6 +264,9 @@ def main():
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: auto)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-events", action="store_true",
+                    help="record an event at every step boundary (per-step times; the event "
+                         "nodes break the programmatic launch edge between steps)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -309,9 +312,8 @@ def main():
     errs = [int(o["err"].item()) for o in outs]
 
     # the timed steps are replayed from CUDA graphs of up to CHUNK steps (a graph of K % CHUNK
-    # steps makes up the rest, so exactly K steps run); a timing event (an event-record graph
-    # node) sits at every step boundary, never between the two kernels of a step (that would
-    # break the programmatic launch edge)
+    # steps makes up the rest, so exactly K steps run); the timed region is bracketed by two
+    # events (per-step events only with --step-events)
     K = args.steps
     CHUNK = min(K, 200)
 
@@ -336,7 +338,7 @@ def main():
         stream.synchronize()
         return g, evs_
 
-    graph, evs = capture(CHUNK, True)
+    graph, evs = capture(CHUNK, args.step_events)
     full, rest = divmod(K, CHUNK)
     graph_rest = capture(rest, False)[0] if rest else None
 

@@ -247,6 +247,9 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
     }
   }
 
+  // a programmatically dependent launch (the next step's verify) may now be scheduled; it
+  // waits for this grid's completion before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (e) atomicOr(&s_err, e);
   __syncthreads();
   if (tid == 0) raise_err(P.err, s_err);

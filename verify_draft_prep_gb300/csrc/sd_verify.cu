@@ -63,7 +63,8 @@ struct VerifyParams {
   float* q_at;
   struct RaceSlot* slots;  // one per request (sampled probability requests)
   int32_t* err;
-  int cl;
+  int cl;   // cluster size: CTAs that share a greedy or logit request's rows
+  int nc;   // CTAs per request (a multiple of cl): sampled probability requests use all of them
   int vec;  // 1: every row starts on a 16-byte boundary
 };
 
@@ -333,18 +334,32 @@ __device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, const P
   constexpr int EPU = Src::EPU, UNR = Src::UNR;
   float a1 = 0.0f, a2 = 0.0f;
   uint32_t best_u = 0xffffffffu;
-  // units [u0, uf) lie inside 16-byte aligned rows: unchecked 128-bit loads, UNR units in flight
+  // units [u0, uf) lie inside 16-byte aligned rows: unchecked 128-bit loads, software-pipelined
+  // so that UNR units are always in flight (each buffer is refilled right after it is consumed)
   const uint32_t uf = src.vec ? max(u0, min(u1, src.full_units())) : u0;
   uint32_t ub = u0 + threadIdx.x;
-  for (; ub + (UNR - 1) * NT < uf; ub += NT * UNR) {
+  if (ub + (UNR - 1) * NT < uf) {
     typename Src::Raw raw[UNR];
 #pragma unroll
     for (int k = 0; k < UNR; ++k) src.fetch_fast(ub + k * NT, raw[k]);
-    uint4 w[UNR][EPU / 4];
+    for (; ub + (2 * UNR - 1) * NT < uf; ub += UNR * NT) {
 #pragma unroll
-    for (int k = 0; k < UNR; ++k) unit_words<Src>(rk, ub + k * NT, rid, j, w[k]);
+      for (int k = 0; k < UNR; ++k) {
+        const uint32_t u = ub + k * NT;
+        uint4 w[EPU / 4];
+        unit_words<Src>(rk, u, rid, j, w);
+        race_take(src, raw[k], w, u, a1, a2, best_u);
+        src.fetch_fast(u + UNR * NT, raw[k]);
+      }
+    }
 #pragma unroll
-    for (int k = 0; k < UNR; ++k) race_take(src, raw[k], w[k], ub + k * NT, a1, a2, best_u);
+    for (int k = 0; k < UNR; ++k) {  // drain the last UNR units in flight
+      const uint32_t u = ub + k * NT;
+      uint4 w[EPU / 4];
+      unit_words<Src>(rk, u, rid, j, w);
+      race_take(src, raw[k], w, u, a1, a2, best_u);
+    }
+    ub += UNR * NT;
   }
   for (; ub < u1; ub += NT) {  // the rest, bounds-checked
     typename Src::Raw raw;
@@ -419,24 +434,33 @@ __device__ uint64_t argmax_chunk(const void* row, uint32_t V, bool vec, uint32_t
   uint32_t bx = 0xffffffffu;
   const uint32_t uf = vec ? max(u0, min(u1, V / EPU)) : u0;
   uint32_t ub = u0 + threadIdx.x;
-  for (; ub + (UNROLL - 1) * NT < uf; ub += NT * UNROLL) {  // unchecked 128-bit loads
+  auto take = [&](const uint4& v, uint32_t u) {
+    const uint32_t x0 = u * EPU;
+    if (DT == SD_F32_PROBS) {
+      argmax_take(__uint_as_float(v.x), x0 + 0, best, bx);
+      argmax_take(__uint_as_float(v.y), x0 + 1, best, bx);
+      argmax_take(__uint_as_float(v.z), x0 + 2, best, bx);
+      argmax_take(__uint_as_float(v.w), x0 + 3, best, bx);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v, i), x0 + i, best, bx);
+    }
+  };
+  auto load = [&](uint32_t u) { return ld_stream_u4((const char*)row + (size_t)u * 16u); };
+  if (ub + (UNROLL - 1) * NT < uf) {  // unchecked 128-bit loads, UNROLL units always in flight
     uint4 v[UNROLL];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k)
-      v[k] = ld_stream_u4((const char*)row + (size_t)(ub + k * NT) * 16u);
+    for (int k = 0; k < UNROLL; ++k) v[k] = load(ub + k * NT);
+    for (; ub + (2 * UNROLL - 1) * NT < uf; ub += UNROLL * NT) {
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) {
-      const uint32_t x0 = (ub + k * NT) * EPU;
-      if (DT == SD_F32_PROBS) {
-        argmax_take(__uint_as_float(v[k].x), x0 + 0, best, bx);
-        argmax_take(__uint_as_float(v[k].y), x0 + 1, best, bx);
-        argmax_take(__uint_as_float(v[k].z), x0 + 2, best, bx);
-        argmax_take(__uint_as_float(v[k].w), x0 + 3, best, bx);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v[k], i), x0 + i, best, bx);
+      for (int k = 0; k < UNROLL; ++k) {
+        take(v[k], ub + k * NT);
+        v[k] = load(ub + (k + UNROLL) * NT);
       }
     }
+#pragma unroll
+    for (int k = 0; k < UNROLL; ++k) take(v[k], ub + k * NT);
+    ub += UNROLL * NT;
   }
   for (; ub < u1; ub += NT) {  // the rest, bounds-checked
     if (DT == SD_F32_PROBS) {
@@ -537,18 +561,28 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
   float ca = 0.0f, cb = 0.0f;
   const uint32_t uf = vec ? max(u0, min(u1, V / 8u)) : u0;
   uint32_t ub = u0 + threadIdx.x;
-  for (; ub + (UNROLL - 1) * NT < uf; ub += NT * UNROLL) {  // unchecked 128-bit loads
+  if (ub + (UNROLL - 1) * NT < uf) {  // unchecked 128-bit loads, UNROLL units always in flight
     uint4 vt[UNROLL], vd[UNROLL];
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       vt[k] = ld_stream_u4(trow + 8u * (ub + k * NT));
       if (HAS_Q) vd[k] = ld_stream_u4(drow + 8u * (ub + k * NT));
     }
+    for (; ub + (2 * UNROLL - 1) * NT < uf; ub += UNROLL * NT) {
+#pragma unroll
+      for (int k = 0; k < UNROLL; ++k) {
+        absorb_unit(a, ca, vt[k], c);
+        if (HAS_Q) absorb_unit(b, cb, vd[k], c);
+        vt[k] = ld_stream_u4(trow + 8u * (ub + (k + UNROLL) * NT));
+        if (HAS_Q) vd[k] = ld_stream_u4(drow + 8u * (ub + (k + UNROLL) * NT));
+      }
+    }
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
       absorb_unit(a, ca, vt[k], c);
       if (HAS_Q) absorb_unit(b, cb, vd[k], c);
     }
+    ub += UNROLL * NT;
   }
   for (; ub < u1; ub += NT) {  // the rest, bounds-checked
     absorb_unit(a, ca, bf16_raw(trow, ub, V, vec), c);
@@ -584,15 +618,16 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ V
   __shared__ Smem sm;
   constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
   using Elt = typename std::conditional<DT == SD_F32_PROBS, float, uint16_t>::type;
-  const int cl = P.cl;
-  const uint32_t crank = blockIdx.x % (unsigned)cl;
-  const int r = (int)(blockIdx.x / (unsigned)cl);
+  // When launched as a programmatic dependent, wait until the preceding grid's writes (possibly
+  // this launch's inputs) are visible; otherwise this returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int nc = P.nc;
+  const uint32_t rank = blockIdx.x % (unsigned)nc;  // this CTA's index within its request
+  const int r = (int)(blockIdx.x / (unsigned)nc);
   const int K = P.K;
   const uint32_t V = (uint32_t)P.V;
   const bool vec = P.vec != 0;
   const uint32_t NU = (V + EPU - 1) / EPU;
-  const uint32_t u0 = (uint32_t)(((uint64_t)NU * crank) / (unsigned)cl);
-  const uint32_t u1 = (uint32_t)(((uint64_t)NU * (crank + 1)) / (unsigned)cl);
   const Elt* tbase = (const Elt*)P.target + (size_t)r * (K + 1) * P.ld_t;
   const Elt* dbase = (const Elt*)P.draft + (size_t)r * K * P.ld_d;
   auto trow = [&](int j) { return tbase + (size_t)j * P.ld_t; };
@@ -600,12 +635,19 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ V
   const int32_t* dr = P.drafts + (size_t)r * K;
   const float T = P.temperature ? P.temperature[r] : 1.0f;
   const bool greedy = (T == 0.0f);
+  const bool sampled_probs = DT == SD_F32_PROBS && !greedy;
+  // Sampled probability requests split their race row over all nc CTAs; greedy and logit
+  // requests use the first cluster only (whole clusters beyond it leave at once).
+  const int cl = sampled_probs ? nc : P.cl;
+  if (rank >= (uint32_t)cl) return;
+  const uint32_t crank = rank;
+  const uint32_t u0 = (uint32_t)(((uint64_t)NU * crank) / (unsigned)cl);
+  const uint32_t u1 = (uint32_t)(((uint64_t)NU * (crank + 1)) / (unsigned)cl);
   int phase = 0;
   int a = K;
   uint32_t b = 0;
   int32_t e = 0;
   bool writer = crank == 0;  // the CTA that writes the request's outputs
-  const bool sampled_probs = DT == SD_F32_PROBS && !greedy;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x < SD_K_MAX) {
@@ -869,22 +911,27 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.slots = (sdk::RaceSlot*)workspace;
   P.err = err;
   P.cl = choose_cluster(V, epu);
+  P.nc = P.cl;  // CTAs per request (measured: a finer split of small batches costs more in
+                // per-CTA accept scans and reductions than it saves in tail)
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
   if (B == 0) return SD_OK;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((long)B * P.cl), 1, 1);
+  cfg.gridDim = dim3((unsigned)((long)B * P.nc), 1, 1);
   cfg.blockDim = dim3(sdk::NT, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)P.cl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // scheduled while the preceding kernel drains; the kernel waits on the device (see above)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t rc;
   if (dtype == SD_F32_PROBS) rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_F32_PROBS>, P);
   else rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_BF16_LOGITS>, P);
