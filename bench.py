@@ -159,11 +159,19 @@ def alloc_outputs(w, device):
                 ws=torch.zeros(max(16, 16 * B), dtype=torch.uint8, device=device))
 
 
+def temperatures(w):
+    """The workload's temperatures, or None when every request samples at T = 1 (the library
+    then needs no per-request temperature and launches only its sampling kernel)."""
+    if not hasattr(w, "_temp_arg"):
+        w._temp_arg = None if bool((w.temperature == 1.0).all()) else w.temperature
+    return w._temp_arg
+
+
 def launch_step(sd, w, o, stream=None):
     """One step: verify, then the fused draft-batch rebuild + hidden gather (a programmatic
     dependent launch of verify)."""
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
-                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream,
+                 temperature=temperatures(w), seed=w.seed, err=o["err"], stream=stream,
                  workspace_buf=o["ws"])
     sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
                          w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
@@ -182,7 +190,7 @@ def launch_prepare(sd, w, o, stream=None):
 
 def launch_verify(sd, w, o, stream=None):
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
-                 temperature=w.temperature, seed=w.seed, err=o["err"], stream=stream,
+                 temperature=temperatures(w), seed=w.seed, err=o["err"], stream=stream,
                  workspace_buf=o["ws"])
 
 

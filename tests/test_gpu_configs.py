@@ -78,10 +78,14 @@ def check_prep(w, res):
     assert np.array_equal(bits(res["out_hidden"]), want)
 
 
-@pytest.mark.parametrize("name,sample", [("small", None), ("b64", None), ("b256mix", None),
-                                         ("b512rag", 96)])
-def test_probs_config_full_size(name, sample):
+@pytest.mark.parametrize("name,sample,null_temp", [("small", None, False), ("b64", None, False),
+                                                   ("b64", None, True), ("b256mix", None, False),
+                                                   ("b512rag", 96, False), ("b512rag", 96, True)])
+def test_probs_config_full_size(name, sample, null_temp):
     w = workloads.make(name, device="cuda")
+    if null_temp:  # every request samples at T = 1: the same results through the NULL path
+        assert bool((w.temperature == 1).all())
+        w.temperature = None
     res = run_step(w)
     req = None
     if sample is not None:

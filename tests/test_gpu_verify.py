@@ -148,3 +148,43 @@ def test_err_pointer_optional_and_stream_order():
                               seed=3)
     assert np.array_equal(outs.cpu().numpy(), want["out_tokens"])
     assert np.array_equal(acc.cpu().numpy(), want["num_accepted"])
+
+
+@pytest.mark.parametrize("B,K,V,seed", [
+    (1, 4, 8192, 20),       # one request spread over every CTA of the grid
+    (3, 5, 20001, 21),      # ragged tail
+    (64, 5, 50000, 22),
+    (700, 2, 9000, 23),     # more requests than CTAs: several segments per CTA
+    (40, 16, 131071, 24),
+])
+def test_all_sampled_path_bit_exact(B, K, V, seed):
+    # temperature NULL: every request samples; the library takes its accept + race kernels
+    rng = np.random.default_rng(300 + seed)
+    p, q, d, _ = random_probs_case(rng, B, K, V, sigma=0.8)
+    got = run_verify(to_dev(p), to_dev(q), to_dev(d), None, seed=seed)
+    want = oracle_verify_rows(torch.from_numpy(p), torch.from_numpy(q), torch.from_numpy(d),
+                              None, seed=seed)
+    assert_verify_equal(got, want)
+
+
+def test_all_sampled_path_edge_cases():
+    rng = np.random.default_rng(25)
+    B, K, V = 12, 4, 10007
+    p, q, d, _ = random_probs_case(rng, B, K, V, zero_frac=0.3)
+    d[0, 0] = V
+    d[1, 1] = -5
+    p3 = p.reshape(B, K + 1, V)
+    q3 = q.reshape(B, K, V)
+    q3[2] = p3[2, :K] * 2          # no residual mass: whole-row fallback on p
+    p3[3] = 0                      # zero request
+    q3[3] = 0
+    got = run_verify(to_dev(p), to_dev(q), to_dev(d), None, seed=99)
+    want = oracle_verify_rows(torch.from_numpy(p), torch.from_numpy(q), torch.from_numpy(d),
+                              None, seed=99)
+    assert want["err"] & oracle.ERR_TOKEN_RANGE and want["err"] & oracle.ERR_ZERO_ROW
+    assert_verify_equal(got, want)
+    # unaligned rows (scalar loads) on the same path
+    pt = torch.zeros(B * (K + 1) * V + 1).cuda()
+    pt[1:] = torch.from_numpy(p).reshape(-1).cuda()
+    got2 = run_verify(pt[1:].view(B * (K + 1), V), to_dev(q), to_dev(d), None, seed=99)
+    assert_verify_equal(got2, want)

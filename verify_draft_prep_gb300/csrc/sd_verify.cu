@@ -37,6 +37,8 @@ namespace sdk {
 constexpr int NT = 256;        // threads per CTA
 constexpr int UNROLL = 4;      // 16-byte units in flight per thread (greedy rows, statistics)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
+constexpr int kMinBlocks = 4;  // resident CTAs per SM the cluster kernel's registers allow
+constexpr int kRaceMinBlocks = 3;  // the same for race_kernel (its loop keeps 4 units in flight)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
 constexpr int kCandCap = 32;            // candidate units evaluated lane-parallel per CTA
 
@@ -64,7 +66,10 @@ struct VerifyParams {
   struct RaceSlot* slots;  // one per request (sampled probability requests)
   int32_t* err;
   int cl;   // cluster size: CTAs that share a greedy or logit request's rows
-  int nc;   // CTAs per request (a multiple of cl): sampled probability requests use all of them
+  int nc;   // CTAs per request in the cluster role (a multiple of cl)
+  int cluster_blocks;  // blocks [0, cluster_blocks) take the cluster role: B * nc
+  int race_blocks;     // blocks after them take the race role (0: sampled requests stay per
+                       // request in the cluster role)
   int vec;  // 1: every row starts on a 16-byte boundary
 };
 
@@ -155,6 +160,44 @@ struct F32Residual {
   }
   __device__ __forceinline__ float at(uint32_t x) const {
     return HAS_Q ? __fsub_rn(__ldg(p + x), __ldg(q + x)) : __ldg(p + x);
+  }
+};
+
+// The same residual source with q chosen at run time (nullptr: the bonus race on p), so that one
+// copy of the race loop serves both cases.
+struct F32ResidualAny {
+  static constexpr int EPU = 4;
+  static constexpr int UNR = 4;
+  const float* p;
+  const float* q;  // nullptr: r = p
+  uint32_t V;
+  bool vec;
+  struct Raw {
+    float p[4], q[4];
+  };
+  __device__ __forceinline__ void fetch(uint32_t u, Raw& raw) const {
+    f32_unit(p, u, V, vec, 0.0f, raw.p);
+    if (q) f32_unit(q, u, V, vec, 0.0f, raw.q);
+    else raw.q[0] = raw.q[1] = raw.q[2] = raw.q[3] = 0.0f;
+  }
+  __device__ __forceinline__ uint32_t full_units() const { return V / 4u; }
+  __device__ __forceinline__ void fetch_fast(uint32_t u, Raw& raw) const {
+    const float4 a = ld_f4(p + 4u * u);
+    raw.p[0] = a.x; raw.p[1] = a.y; raw.p[2] = a.z; raw.p[3] = a.w;
+    if (q) {
+      const float4 b = ld_f4(q + 4u * u);
+      raw.q[0] = b.x; raw.q[1] = b.y; raw.q[2] = b.z; raw.q[3] = b.w;
+    } else {
+      raw.q[0] = raw.q[1] = raw.q[2] = raw.q[3] = 0.0f;
+    }
+  }
+  // p - 0 == p exactly, so the bonus race sees r = p as the definition asks
+  __device__ __forceinline__ void residual(const Raw& raw, float (&r)[4]) const {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __fsub_rn(raw.p[i], raw.q[i]);
+  }
+  __device__ __forceinline__ float at(uint32_t x) const {
+    return q ? __fsub_rn(__ldg(p + x), __ldg(q + x)) : __ldg(p + x);
   }
 };
 
@@ -329,7 +372,8 @@ __device__ __forceinline__ void race_take(const Src& src, const typename Src::Ra
 // Exact race winner over units [u0, u1) of one row: the CTA's packed (key, ~x) maximum, or 0 when
 // no element of the chunk has a positive residual.
 template <class Src>
-__device__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1, const PhiloxRoundKeys& rk,
+__device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1,
+                                               const PhiloxRoundKeys& rk,
                                uint32_t rid, uint32_t j, Smem& sm) {
   constexpr int EPU = Src::EPU, UNR = Src::UNR;
   float a1 = 0.0f, a2 = 0.0f;
@@ -612,9 +656,198 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
   sd = b;
 }
 
+// -------------------------------------------------------- sampled probability requests (shared)
+// Accept scan of request r by one warp (lane j checks draft d_{j+1}); P/Q of the examined drafts
+// go to Ps/Qs (others stay as they are). Returns a_r; *bad_out receives SD_ERR_TOKEN_RANGE when
+// the first rejection came from an out-of-range draft.
+__device__ int accept_scan_warp(const VerifyParams& P, int r, float* Ps, float* Qs, int* bad_out) {
+  const int K = P.K;
+  const uint32_t V = (uint32_t)P.V;
+  const int j = threadIdx.x & 31;
+  const float* trow = (const float*)P.target + ((size_t)r * (K + 1) + j) * P.ld_t;
+  const float* drow = (const float*)P.draft + ((size_t)r * K + j) * P.ld_d;
+  bool acc = false, bad = false;
+  float Pv = 0.0f, Qv = 0.0f;
+  if (j < K) {
+    const int d = __ldg(P.drafts + (size_t)r * K + j);
+    if (d >= 0 && (uint32_t)d < V) {
+      Pv = __ldg(trow + d);
+      Qv = __ldg(drow + d);
+      const double u = accept_uniform(P.rk, (uint32_t)r, (uint32_t)j);
+      acc = u * (double)Qv < (double)Pv;  // u*Q is exact in double
+    } else {
+      bad = true;
+    }
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, j < K && !acc);
+  const int av = rej ? __ffs(rej) - 1 : K;
+  if (j < K && j <= av) {
+    Ps[j] = Pv;
+    Qs[j] = Qv;
+  }
+  const unsigned badm = __ballot_sync(0xffffffffu, bad && j == av);
+  *bad_out = badm ? SD_ERR_TOKEN_RANGE : 0;
+  return av;
+}
+
+// Outputs of one request: d_1..d_a, b, -1 padding, a, P/Q at the drafts (the whole CTA writes).
+__device__ void write_request(const VerifyParams& P, int r, int a, uint32_t b, int32_t e,
+                              const float* Ps, const float* Qs) {
+  const int K = P.K;
+  const int t = threadIdx.x;
+  if (t <= K) {
+    int32_t tok = -1;
+    if (t < a) tok = __ldg(P.drafts + (size_t)r * K + t);
+    else if (t == a) tok = (int32_t)b;
+    P.out_tokens[(size_t)r * (K + 1) + t] = tok;
+  }
+  if (t < K) {
+    if (P.p_at) P.p_at[(size_t)r * K + t] = Ps[t];
+    if (P.q_at) P.q_at[(size_t)r * K + t] = Qs[t];
+  }
+  if (t == 0) {
+    P.num_accepted[r] = a;
+    raise_err(P.err, e);
+  }
+}
+
+// Merge a CTA's packed race maximum over `units` units of request r's race row into its slot.
+// Returns (in every thread) whether this CTA completed the row, and then the row's maximum.
+__device__ bool merge_slot(RaceSlot* slot, uint64_t pk, uint32_t units, uint32_t row_units,
+                           Smem& sm, uint64_t& row_max) {
+  if (threadIdx.x == 0) {
+    if (pk) atomicMax(&slot->best, (unsigned long long)pk);
+    __threadfence();
+    const unsigned prev = atomicAdd(&slot->count, units);
+    const bool last = prev + units == row_units;
+    sm.last = last;
+    if (last) {
+      __threadfence();
+      sm.bcast = atomicOr(&slot->best, 0ull);  // every other part of the row is merged by now
+    }
+  }
+  __syncthreads();
+  const bool last = sm.last != 0;
+  row_max = sm.bcast;
+  __syncthreads();
+  return last;
+}
+
+// The CTA that completed request r's race row: fallback and outputs, then the slot is zeroed.
+__device__ __noinline__ void finish_sampled(const VerifyParams& P, int r, int a, int32_t e,
+                                            uint64_t pk,
+                               const float* Ps, const float* Qs, Smem& sm) {
+  const int K = P.K;
+  const uint32_t V = (uint32_t)P.V;
+  const uint32_t NU = (V + 3u) / 4u;
+  const bool vec = P.vec != 0;
+  const int jr = a < K ? a : K;
+  const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
+  if (packed_key_bits(pk) == 0u && a < K) {
+    // no positive residual key anywhere in the row: race on p of the same row, whole row
+    F32Residual<false> src{prow, nullptr, V, vec};
+    pk = race_chunk(src, 0u, NU, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+  }
+  uint32_t b = 0;
+  if (packed_key_bits(pk) == 0u) e |= SD_ERR_ZERO_ROW;
+  else b = packed_index(pk);
+  if (threadIdx.x == 0) {
+    P.slots[r].best = 0ull;
+    P.slots[r].count = 0u;
+  }
+  write_request(P, r, a, b, e, Ps, Qs);
+}
+
+// Accept phase of an all-sampled batch: one warp per request. Writes num_accepted, the accepted
+// drafts and the -1 padding of out_tokens (the final token's place is left to the race phase),
+// P/Q at the drafts and the out-of-range error bit.
+__global__ void __launch_bounds__(NT) accept_kernel(const __grid_constant__ VerifyParams P) {
+  __shared__ float Ps[NT / 32][SD_K_MAX], Qs[NT / 32][SD_K_MAX];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (NT / 32) + warp;
+  if (r >= P.B) return;  // warp-uniform
+  const int K = P.K;
+  if (lane < SD_K_MAX) {
+    Ps[warp][lane] = -1.0f;
+    Qs[warp][lane] = -1.0f;
+  }
+  __syncwarp();
+  int bad;
+  const int a = accept_scan_warp(P, r, Ps[warp], Qs[warp], &bad);
+  __syncwarp();
+  if (lane <= K && lane != a) {
+    P.out_tokens[(size_t)r * (K + 1) + lane] =
+        lane < a ? __ldg(P.drafts + (size_t)r * K + lane) : -1;
+  }
+  if (lane < K) {
+    if (P.p_at) P.p_at[(size_t)r * K + lane] = Ps[warp][lane];
+    if (P.q_at) P.q_at[(size_t)r * K + lane] = Qs[warp][lane];
+  }
+  if (lane == 0) {
+    P.num_accepted[r] = a;
+    raise_err(P.err, bad);
+  }
+}
+
+// The CTA that completed request r's race row (race phase): fallback, the final token, slot reset.
+__device__ __noinline__ void finish_race(const VerifyParams& P, int r, int a, uint64_t pk,
+                                         Smem& sm) {
+  const int K = P.K;
+  const uint32_t V = (uint32_t)P.V;
+  const uint32_t NU = (V + 3u) / 4u;
+  const int jr = a < K ? a : K;
+  const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
+  if (packed_key_bits(pk) == 0u && a < K) {
+    // no positive residual key anywhere in the row: race on p of the same row, whole row
+    F32Residual<false> src{prow, nullptr, V, P.vec != 0};
+    pk = race_chunk(src, 0u, NU, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+  }
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    if (packed_key_bits(pk) == 0u) raise_err(P.err, SD_ERR_ZERO_ROW);
+    else b = packed_index(pk);
+    P.out_tokens[(size_t)r * (K + 1) + a] = (int32_t)b;
+    P.slots[r].best = 0ull;
+    P.slots[r].count = 0u;
+  }
+}
+
+// Race phase of an all-sampled batch: the requests' race rows laid end to end (unit u of request
+// r at position r*NU + u) and that line split evenly over race_blocks CTAs (a whole number per
+// SM). Every unit costs the same Philox and filter arithmetic, and that, more than the one or
+// two rows a unit reads, sets a CTA's time (measured: balancing by bytes instead was slower), so
+// every SM gets the same number of units. A CTA covers one or a few request segments; the CTA
+// that completes a row finishes its request.
+__device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Smem& sm) {
+  const int K = P.K;
+  const uint32_t V = (uint32_t)P.V;
+  const uint32_t NU = (V + 3u) / 4u;
+  const bool vec = P.vec != 0;
+  const unsigned long long W = (unsigned long long)P.B * NU;
+  const unsigned long long w0 = W * c / (unsigned)P.race_blocks;
+  const unsigned long long w1 = W * (c + 1) / (unsigned)P.race_blocks;
+  if (w1 <= w0) return;  // CTA-uniform
+  const int r0 = (int)(w0 / NU), r1 = (int)((w1 - 1) / NU);  // at most kMaxSeg requests
+  for (int r = r0; r <= r1; ++r) {
+    const unsigned long long base = (unsigned long long)r * NU;
+    const uint32_t lo = (uint32_t)(max(w0, base) - base);
+    const uint32_t hi = (uint32_t)(min(w1, base + NU) - base);
+    const int a = P.num_accepted[r];
+    const int jr = a < K ? a : K;
+    const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
+    const float* qrow = a < K ? (const float*)P.draft + ((size_t)r * K + jr) * P.ld_d : nullptr;
+    const F32ResidualAny src{prow, qrow, V, vec};
+    const uint64_t pk = race_chunk(src, lo, hi, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+    uint64_t row_max;
+    if (merge_slot(P.slots + r, pk, hi - lo, NU, sm, row_max)) finish_race(P, r, a, row_max, sm);
+  }
+}
+
 // ---------------------------------------------------------------------------------- the kernel
 template <int DT>
-__global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ VerifyParams P) {
+__global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_constant__ VerifyParams P) {
   __shared__ Smem sm;
   constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
   using Elt = typename std::conditional<DT == SD_F32_PROBS, float, uint16_t>::type;
@@ -638,6 +871,8 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ V
   const bool sampled_probs = DT == SD_F32_PROBS && !greedy;
   // Sampled probability requests split their race row over all nc CTAs; greedy and logit
   // requests use the first cluster only (whole clusters beyond it leave at once).
+  // sampled probability requests belong to race_kernel when it is launched
+  if (sampled_probs && P.race_blocks > 0) return;
   const int cl = sampled_probs ? nc : P.cl;
   if (rank >= (uint32_t)cl) return;
   const uint32_t crank = rank;
@@ -690,33 +925,14 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ V
       }
     }
   } else if (DT == SD_F32_PROBS) {
-    // ---- sampled, probability rows: scalar accept scan, then one race row
+    // ---- sampled, probability rows (small vocabularies): scalar accept scan, then the CTA's
+    // share of the one race row, merged through the request's slot
     if (threadIdx.x < 32) {
-      const int j = lane;
-      bool acc = false;
-      bool bad = false;
-      float Pv = 0.0f, Qv = 0.0f;
-      if (j < K) {
-        const int d = __ldg(dr + j);
-        if (d >= 0 && (uint32_t)d < V) {
-          Pv = __ldg((const float*)trow(j) + d);
-          Qv = __ldg((const float*)drow(j) + d);
-          const double u = accept_uniform(P.rk, (uint32_t)r, (uint32_t)j);
-          acc = u * (double)Qv < (double)Pv;  // u*Q is exact in double
-        } else {
-          bad = true;
-        }
-      }
-      const unsigned rej = __ballot_sync(0xffffffffu, j < K && !acc);
-      const int av = rej ? __ffs(rej) - 1 : K;
-      if (j < K && j <= av) {
-        sm.P[j] = Pv;
-        sm.Q[j] = Qv;
-      }
-      const unsigned badm = __ballot_sync(0xffffffffu, bad && j == av);
+      int bad;
+      const int av = accept_scan_warp(P, r, sm.P, sm.Q, &bad);
       if (lane == 0) {
         sm.a = av;
-        sm.e = badm ? SD_ERR_TOKEN_RANGE : 0;
+        sm.e = bad;
       }
     }
     __syncthreads();
@@ -731,40 +947,10 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ V
       F32Residual<false> src{(const float*)trow(jr), nullptr, V, vec};
       pk = race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm);
     }
-    // Merge into the request's slot; the CTA that merges last finishes the request. No CTA
-    // waits for another.
-    RaceSlot* slot = P.slots + r;
-    if (threadIdx.x == 0) {
-      if (pk) atomicMax(&slot->best, (unsigned long long)pk);
-      __threadfence();
-      const unsigned prev = atomicAdd(&slot->count, 1u);
-      sm.last = (prev == (unsigned)cl - 1u);
-    }
-    __syncthreads();
-    writer = sm.last != 0;
-    if (writer) {
-      if (threadIdx.x == 0) {
-        __threadfence();
-        sm.bcast = atomicOr(&slot->best, 0ull);  // every other CTA's maximum is in by now
-      }
-      __syncthreads();
-      pk = sm.bcast;
-      if (packed_key_bits(pk) == 0u && a < K) {
-        // no positive residual key anywhere in the row: race on p of the same row, whole row
-        F32Residual<false> src{(const float*)trow(jr), nullptr, V, vec};
-        pk = race_chunk(src, 0u, NU, P.rk, (uint32_t)r, (uint32_t)jr, sm);
-      }
-      if (packed_key_bits(pk) == 0u) {
-        e |= SD_ERR_ZERO_ROW;
-        b = 0;
-      } else {
-        b = packed_index(pk);
-      }
-      if (threadIdx.x == 0) {
-        slot->best = 0ull;
-        slot->count = 0u;
-      }
-    }
+    uint64_t row_max;
+    if (merge_slot(P.slots + r, pk, u1 - u0, NU, sm, row_max))
+      finish_sampled(P, r, a, e, row_max, sm.P, sm.Q, sm);
+    writer = false;  // finish_sampled wrote the outputs (in the CTA that completed the row)
   } else {
     // ---- sampled, bf16 logit rows: per row max/sum, decide, race on the rejected row
     const float c = 1.4426950408889634f / T;
@@ -866,6 +1052,16 @@ __global__ void __launch_bounds__(NT, 4) verify_kernel(const __grid_constant__ V
   if (cl > 1 && !sampled_probs) cluster_barrier();
 }
 
+// Sampled probability requests with large vocabularies: the race role over a whole number of
+// CTAs per SM (see race_role).
+__global__ void __launch_bounds__(NT, kRaceMinBlocks)
+    race_kernel(const __grid_constant__ VerifyParams P) {
+  __shared__ Smem sm;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  race_role(P, blockIdx.x, sm);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace sdk
 
 // ------------------------------------------------------------------------------------ launcher
@@ -876,6 +1072,20 @@ namespace {
 extern "C" size_t sd_verify_workspace_launch(int B) { return (size_t)B * sizeof(sdk::RaceSlot); }
 
 namespace {
+
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cached[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 152;
+  int n = cached[dev].load();
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 152;
+    cached[dev].store(n);
+  }
+  return n;
+}
 
 int choose_cluster(int V, int epu) {
   const long units = ((long)V + epu - 1) / epu;
@@ -911,14 +1121,25 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.slots = (sdk::RaceSlot*)workspace;
   P.err = err;
   P.cl = choose_cluster(V, epu);
-  P.nc = P.cl;  // CTAs per request (measured: a finer split of small batches costs more in
-                // per-CTA accept scans and reductions than it saves in tail)
+  P.nc = P.cl;  // CTAs per request in the cluster role
+  P.cluster_blocks = B * P.nc;
+  // An all-sampled batch (temperature NULL) on large probability rows whose cluster grid would
+  // span several waves takes the accept phase and then the race phase over a whole number of
+  // CTAs per SM; smaller batches stay in the one cluster kernel (measured faster for them).
+  P.race_blocks = 0;
+  if (dtype == SD_F32_PROBS && (V + 3) / 4 >= 2048 && temperature == nullptr &&
+      (long)B * P.nc >= 2L * sdk::kMinBlocks * sm_count()) {
+    // a CTA's share spans at most B/g + 2 requests: g >= B/6 keeps that within 8
+    int g = sdk::kRaceMinBlocks * sm_count();
+    if (g < (B + 5) / 6) g = (B + 5) / 6;
+    P.race_blocks = g;
+  }
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
   if (B == 0) return SD_OK;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((long)B * P.nc), 1, 1);
+  cfg.gridDim = dim3((unsigned)P.cluster_blocks, 1, 1);
   cfg.blockDim = dim3(sdk::NT, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -932,9 +1153,40 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t rc;
-  if (dtype == SD_F32_PROBS) rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_F32_PROBS>, P);
-  else rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_BF16_LOGITS>, P);
+  cudaError_t rc = cudaSuccess;
+  if (P.race_blocks == 0) {
+    // one kernel: clusters per request (greedy and logit rows in order; sampled probability
+    // rows split over the request's CTAs)
+    if (dtype == SD_F32_PROBS) rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_F32_PROBS>, P);
+    else rc = cudaLaunchKernelEx(&cfg, sdk::verify_kernel<SD_BF16_LOGITS>, P);
+    return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+  }
+  {
+    // every request sampled on probability rows: the accept phase, then the race phase balanced
+    // by bytes over the whole GPU (both programmatic dependents of what precedes them)
+    cudaLaunchConfig_t acfg = {};
+    acfg.gridDim = dim3((unsigned)((B + sdk::NT / 32 - 1) / (sdk::NT / 32)), 1, 1);
+    acfg.blockDim = dim3(sdk::NT, 1, 1);
+    acfg.stream = stream;
+    cudaLaunchAttribute aattr[1];
+    aattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    aattr[0].val.programmaticStreamSerializationAllowed = 1;
+    acfg.attrs = aattr;
+    acfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&acfg, sdk::accept_kernel, P) != cudaSuccess) return SD_E_LAUNCH;
+  }
+  {
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3((unsigned)P.race_blocks, 1, 1);
+    rcfg.blockDim = dim3(sdk::NT, 1, 1);
+    rcfg.stream = stream;
+    cudaLaunchAttribute rattr[1];
+    rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    rattr[0].val.programmaticStreamSerializationAllowed = 1;
+    rcfg.attrs = rattr;
+    rcfg.numAttrs = 1;
+    rc = cudaLaunchKernelEx(&rcfg, sdk::race_kernel, P);
+  }
   return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
 }
 
