@@ -306,6 +306,8 @@ def main():
     nsets = args.sets or (4 if cfg["B"] * cfg["V"] < 64 * 201088 * 2 else 2)
     sets = [w0] + make_sets(args.config, nsets - 1, device, rank + 1)
     outs = [alloc_outputs(w, device) for w in sets]
+    for w in sets:
+        temperatures(w)  # decided before any graph capture (it reads the device)
 
     # warm-up (untimed), then algorithmic bytes from each set's accepted counts
     stream = torch.cuda.Stream(device)

@@ -38,7 +38,7 @@ constexpr int NT = 256;        // threads per CTA
 constexpr int UNROLL = 4;      // 16-byte units in flight per thread (greedy rows, statistics)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
 constexpr int kMinBlocks = 4;  // resident CTAs per SM the cluster kernel's registers allow
-constexpr int kRaceMinBlocks = 3;  // the same for race_kernel (its loop keeps 4 units in flight)
+constexpr int kRaceMinBlocks = 4;  // the same for race_kernel (its loop keeps 3 units in flight)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
 constexpr int kCandCap = 32;            // candidate units evaluated lane-parallel per CTA
 
@@ -167,7 +167,7 @@ struct F32Residual {
 // copy of the race loop serves both cases.
 struct F32ResidualAny {
   static constexpr int EPU = 4;
-  static constexpr int UNR = 4;
+  static constexpr int UNR = 3;
   const float* p;
   const float* q;  // nullptr: r = p
   uint32_t V;
