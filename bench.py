@@ -170,9 +170,7 @@ def temperatures(w):
 def launch_step(sd, w, o, stream=None):
     """One step: verify, then the fused draft-batch rebuild + hidden gather (a programmatic
     dependent launch of verify)."""
-    sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
-                 temperature=temperatures(w), seed=w.seed, err=o["err"], stream=stream,
-                 workspace_buf=o["ws"])
+    launch_verify(sd, w, o, stream)
     sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
                          w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
                          o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
@@ -189,9 +187,10 @@ def launch_prepare(sd, w, o, stream=None):
 
 
 def launch_verify(sd, w, o, stream=None):
+    # request_base: this rank's shard starts at request rank * B of the job's global batch
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
                  temperature=temperatures(w), seed=w.seed, err=o["err"], stream=stream,
-                 workspace_buf=o["ws"])
+                 workspace_buf=o["ws"], request_base=getattr(w, "request_base", 0))
 
 
 def time_graph(fn, sets, outs, stream, K):
@@ -300,6 +299,7 @@ def main():
 
     sd.load()
     import workloads
+    from verify_draft_prep_gb300 import shard
 
     cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
     w0 = workloads.make(args.config, device=device, gen_seed=1000 + 7919 * rank)
@@ -308,6 +308,9 @@ def main():
     outs = [alloc_outputs(w, device) for w in sets]
     for w in sets:
         temperatures(w)  # decided before any graph capture (it reads the device)
+        # each rank holds its own shard of the job's batch: requests rank*B .. rank*B + B - 1 in
+        # the Philox counters (weak scaling, no exchange on the data path)
+        w.request_base = shard.request_base(w.B)[0] if world > 1 else 0
 
     # warm-up (untimed), then algorithmic bytes from each set's accepted counts
     stream = torch.cuda.Stream(device)
@@ -382,7 +385,7 @@ def main():
 
     B = sets[0].B
     ms_per_step = total_ms / K
-    value = world * B * K / (total_ms / 1e3)
+    value = shard.whole_job_rate(B * K, world, total_ms)
     bytes_v = float(np.mean([per_set[s % nsets][0] for s in range(CHUNK)]))
     bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(CHUNK)]))
     peak, peak_kind = _peaks()
@@ -396,6 +399,9 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(host_copy(sets[0]))
 
+    # kernels per step: the verify call's (one, or accept + race) and the fused rebuild's one
+    launches = sd.sd_verify_kernels(B, sets[0].V, 0 if cfg["kind"] == "probs" else 1,
+                                    temperatures(sets[0]) is not None) + 1
     a_all = np.concatenate([p[3] for p in per_set])
     info = {
         "verify_ms": avg_v, "prepare_ms": avg_p,
@@ -419,13 +425,13 @@ def main():
                        "timing": "one CUDA graph of all timed steps (verify, then the fused "
                                  "rebuild as its programmatic dependent); the verify kernel "
                                  "alone in a second graph for the roofline",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"dp{world}: request shards of {B} per GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "sd_verify", "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": bytes_v,
                          "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clk,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * K, "clocks": clk,
         }
         print(json.dumps(line))
     if world > 1:
@@ -457,6 +463,8 @@ def run_e2e(sd, w, device, steps):
         setattr(wd, k, v)
     for k, v in dev.items():
         setattr(wd, k, v)
+    if getattr(w, "_temp_arg", None) is not None:
+        wd._temp_arg = dev["temperature"]  # the copy made inside each step, not set 0's tensor
     stream = torch.cuda.Stream(device)
 
     def step():
@@ -477,7 +485,15 @@ def run_e2e(sd, w, device, steps):
         e.record(stream)
         stream.synchronize()
     ms = s.elapsed_time(e) / steps
-    return {"value": w.B / (ms * 1e-3), "unit": "requests/s", "h2d_bytes_per_step": h2d,
+    world = 1
+    import torch.distributed as dist
+
+    if dist.is_initialized():  # the job's rate: every rank's requests over the slowest rank
+        world = dist.get_world_size()
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * w.B / (ms * 1e-3), "unit": "requests/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
 
 

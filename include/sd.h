@@ -95,7 +95,12 @@ extern "C" {
  *   target [B*(K+1) rows, stride ld_t elements], draft [B*K rows, stride ld_d elements]
  *     (fp32 or bf16 per dtype; ld >= V). Rows whose start is 16-byte aligned are read with
  *     128-bit loads, other layouts with scalar loads.
- *   drafts [B, K] int32; temperature [B] fp32 or NULL; seed: Philox key.
+ *   drafts [B, K] int32; temperature [B] fp32 or NULL (every request samples at T = 1; for
+ *     large probability rows the library then balances the race over the whole GPU);
+ *   seed: Philox key; request_base: the request index that local request 0 has in the Philox
+ *     counters (r in the blocks above is request_base + local index), so that a batch split
+ *     over several GPUs by request draws exactly what one GPU would draw for the whole batch;
+ *     request_base + B <= 2^32.
  * Outputs:
  *   out_tokens [B, K+1] int32: d_1..d_{a_r}, b_r, then -1.
  *   num_accepted [B] int32: a_r.
@@ -108,9 +113,10 @@ extern "C" {
  */
 SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t,
                      const void* draft, long ld_d, const int32_t* drafts,
-                     const float* temperature, uint64_t seed, int32_t* out_tokens,
-                     int32_t* num_accepted, float* p_at_draft, float* q_at_draft, void* workspace,
-                     size_t workspace_bytes, int32_t* err, void* stream);
+                     const float* temperature, uint64_t seed, uint32_t request_base,
+                     int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft,
+                     float* q_at_draft, void* workspace, size_t workspace_bytes, int32_t* err,
+                     void* stream);
 
 /*
  * Size in bytes of the workspace sd_verify needs for B requests: 16 bytes per request, where the
@@ -119,6 +125,16 @@ SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld
  * concurrently need separate workspaces.
  */
 SD_API size_t sd_verify_workspace_bytes(int B, int K, int V, int dtype);
+
+/*
+ * Number of kernels one sd_verify (or sd_verify_noalloc) call with these sizes launches on the
+ * current device: 0 for B == 0; 2 when every request samples (has_temperature == 0) on large
+ * probability rows and the batch fills the GPU several times (an accept kernel, then a race
+ * kernel balanced over all SMs); 1 otherwise. A planning query for callers that count launches
+ * (a CUDA-graph budget, a profiler filter); it launches nothing. Returns a negative status for
+ * an unknown dtype or B < 0, V < 1.
+ */
+SD_API int sd_verify_kernels(int B, int V, int dtype, int has_temperature);
 
 /*
  * sd_verify_noalloc -- sd_verify for callers that cannot allocate device memory. This call has
@@ -139,9 +155,9 @@ SD_API size_t sd_verify_workspace_bytes(int B, int K, int V, int dtype);
 #define SD_VERIFY_NOALLOC_MAX_B 4096
 SD_API int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target, long ld_t,
                              const void* draft, long ld_d, const int32_t* drafts,
-                             const float* temperature, uint64_t seed, int32_t* out_tokens,
-                             int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
-                             int32_t* err, void* stream);
+                             const float* temperature, uint64_t seed, uint32_t request_base,
+                             int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft,
+                             float* q_at_draft, int32_t* err, void* stream);
 
 /*
  * sd_pdraft_expand -- rebuild of the drafter batch for P-EAGLE parallel drafting.

@@ -17,7 +17,7 @@ def to_dev(a, dtype=None):
     return t.to(DEV)
 
 
-def run_verify(target, draft, drafts, temperature=None, seed=0):
+def run_verify(target, draft, drafts, temperature=None, seed=0, request_base=0):
     """target [B*(K+1), V], draft [B*K, V] device tensors (fp32 or bf16)."""
     B, K = drafts.shape
     dev = target.device
@@ -28,7 +28,7 @@ def run_verify(target, draft, drafts, temperature=None, seed=0):
                err=torch.zeros(1, dtype=torch.int32, device=dev))
     sd.sd_verify(target, draft, drafts, out["out_tokens"], out["num_accepted"],
                  temperature=temperature, seed=seed, p_at_draft=out["p_at_draft"],
-                 q_at_draft=out["q_at_draft"], err=out["err"])
+                 q_at_draft=out["q_at_draft"], err=out["err"], request_base=request_base)
     torch.cuda.synchronize()
     res = {k: v.cpu().numpy() for k, v in out.items()}
     res["err"] = int(res["err"][0])

@@ -41,18 +41,25 @@ def test_internal_symbols_are_hidden(lib):
 def test_host_argument_checks(lib):
     P = None
     # K out of range, V < 1, ld < V, bad dtype
-    assert lib.sd_verify(1, 0, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == -2
-    assert lib.sd_verify(1, 17, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == -2
-    assert lib.sd_verify(1, 2, 0, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == -2
-    assert lib.sd_verify(1, 2, 10, 0, P, 9, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == -2
-    assert lib.sd_verify(1, 2, 10, 7, P, 10, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == -3
+    assert lib.sd_verify(1, 0, 10, 0, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == -2
+    assert lib.sd_verify(1, 17, 10, 0, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == -2
+    assert lib.sd_verify(1, 2, 0, 0, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == -2
+    assert lib.sd_verify(1, 2, 10, 0, P, 9, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == -2
+    assert lib.sd_verify(1, 2, 10, 7, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == -3
     # null rows
-    assert lib.sd_verify(1, 2, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == -1
+    assert lib.sd_verify(1, 2, 10, 0, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == -1
     # a workspace smaller than sd_verify_workspace_bytes is refused
     assert lib.sd_verify_workspace_bytes(64, 5, 201088, 0) == 64 * 16
-    assert lib.sd_verify(4, 2, 10, 0, 16, 10, 16, 10, 16, P, 0, 16, 16, P, P, 16, 63, P, P) == -2
+    assert lib.sd_verify(4, 2, 10, 0, 16, 10, 16, 10, 16, P, 0, 0, 16, 16, P, P, 16, 63, P, P) == -2
+    # request_base + B beyond the 32-bit Philox request index
+    assert lib.sd_verify(4, 2, 10, 0, 16, 10, 16, 10, 16, P, 0, 2**32 - 3, 16, 16, P, P, 16, 64, P,
+                         P) == -2
+    # the launch-count query checks its arguments before it looks at the device
+    assert lib.sd_verify_kernels(4, 10, 7, 0) == -3
+    assert lib.sd_verify_kernels(-1, 10, 0, 0) == -2
+    assert lib.sd_verify_kernels(0, 10, 0, 0) == 0
     # an empty batch is a no-op
-    assert lib.sd_verify(0, 2, 10, 0, P, 10, P, 10, P, P, 0, P, P, P, P, P, 0, P, P) == 0
+    assert lib.sd_verify(0, 2, 10, 0, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == 0
     # expand: block size 0, null outputs
     assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 0, 0, 4, *([P] * 11)) == -2
     assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 16, 0, 4, *([P] * 11)) == -1

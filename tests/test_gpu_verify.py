@@ -188,3 +188,29 @@ def test_all_sampled_path_edge_cases():
     pt[1:] = torch.from_numpy(p).reshape(-1).cuda()
     got2 = run_verify(pt[1:].view(B * (K + 1), V), to_dev(q), to_dev(d), None, seed=99)
     assert_verify_equal(got2, want)
+
+
+@pytest.mark.parametrize("temperature", ["mixed", None])
+def test_request_base_shards_reproduce_the_whole_batch(temperature):
+    # a batch verified as two shards, each with request_base = its first request's index,
+    # gives bit for bit what one call over the whole batch gives (both kernel paths)
+    rng = np.random.default_rng(31)
+    B, K, V = 10, 4, 30011
+    p, q, d, T = random_probs_case(rng, B, K, V, greedy_frac=0.3 if temperature else 0.0)
+    T = to_dev(T) if temperature else None
+    pt, qt, dt = to_dev(p), to_dev(q), to_dev(d)
+    whole = run_verify(pt, qt, dt, T, seed=7)
+    s = 3
+    lo = run_verify(pt[:s * (K + 1)], qt[:s * K], dt[:s], None if T is None else T[:s], seed=7)
+    hi = run_verify(pt[s * (K + 1):], qt[s * K:], dt[s:], None if T is None else T[s:], seed=7,
+                    request_base=s)
+    for k in ("out_tokens", "num_accepted", "p_at_draft", "q_at_draft"):
+        assert np.array_equal(np.concatenate([lo[k], hi[k]]).view(np.int32),
+                              whole[k].view(np.int32)), k
+    want = oracle_verify_rows(torch.from_numpy(p), torch.from_numpy(q), torch.from_numpy(d),
+                              None if T is None else T.cpu(), seed=7, req_ids=np.arange(s, B))
+    assert_verify_equal(hi, want, check_err=False)
+    # a shard without request_base draws other numbers: the shifted counters matter
+    if temperature is None:
+        shifted = run_verify(pt[s * (K + 1):], qt[s * K:], dt[s:], None, seed=7)
+        assert not np.array_equal(shifted["out_tokens"], hi["out_tokens"])

@@ -32,7 +32,7 @@ def _noalloc_call(lib, w, o, dtype):
     stream = torch.cuda.current_stream().cuda_stream
     return lib.sd_verify_noalloc(B, K, V, dtype, w.target.data_ptr(), w.target.stride(0),
                                  w.draft.data_ptr(), w.draft.stride(0), w.drafts.data_ptr(),
-                                 w.temperature.data_ptr(), w.seed, o["out_tokens"].data_ptr(),
+                                 w.temperature.data_ptr(), w.seed, 0, o["out_tokens"].data_ptr(),
                                  o["num_accepted"].data_ptr(), o["p_at"].data_ptr(),
                                  o["q_at"].data_ptr(), o["err"].data_ptr(), stream)
 
@@ -64,11 +64,11 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     lib = sd.load()
     B = sd.SD_VERIFY_NOALLOC_MAX_B + 1
     P = None
-    rc = lib.sd_verify_noalloc(B, 2, 10, sd.SD_F32_PROBS, P, 10, P, 10, P, P, 0, P, P, P, P, P,
-                               P)
+    rc = lib.sd_verify_noalloc(B, 2, 10, sd.SD_F32_PROBS, P, 10, P, 10, P, P, 0, 0, P, P, P, P,
+                               P, P)
     assert rc == -7
     assert b"SD_VERIFY_NOALLOC_MAX_B" in lib.sd_status_string(rc)
-    assert lib.sd_verify_noalloc(0, 2, 10, sd.SD_F32_PROBS, P, 10, P, 10, P, P, 0, P, P, P, P, P,
-                                 P) == 0
+    assert lib.sd_verify_noalloc(0, 2, 10, sd.SD_F32_PROBS, P, 10, P, 10, P, P, 0, 0, P, P, P, P,
+                                 P, P) == 0
     _ = ctypes  # the entry point is called through the C ABI above
     assert np.int32(rc) == -7

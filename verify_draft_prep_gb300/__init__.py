@@ -29,7 +29,8 @@ SD_ERR_MAP_RANGE = 8
 SD_ERR_ZERO_ROW = 16
 SD_ERR_TOTAL_RANGE = 32
 
-EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_noalloc", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
+            "sd_verify_noalloc", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -51,14 +52,16 @@ def load():
         lib = ctypes.CDLL(LIB_PATH)
         P, i32, i64, u32, u64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_long, ctypes.c_uint32,
                                  ctypes.c_uint64)
-        lib.sd_verify.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, P, P, P, P, P,
-                                  ctypes.c_size_t, P, P]
+        lib.sd_verify.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, u32, P, P, P,
+                                  P, P, ctypes.c_size_t, P, P]
         lib.sd_verify.restype = i32
-        lib.sd_verify_noalloc.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, P, P,
-                                          P, P, P, P]
+        lib.sd_verify_noalloc.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, u32, P,
+                                          P, P, P, P, P]
         lib.sd_verify_noalloc.restype = i32
         lib.sd_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.sd_verify_workspace_bytes.restype = ctypes.c_size_t
+        lib.sd_verify_kernels.argtypes = [i32, i32, i32, i32]
+        lib.sd_verify_kernels.restype = i32
         lib.sd_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32, i32,
                                          P, P, P, P, P, P, P, P, P, P, P]
         lib.sd_pdraft_expand.restype = i32
@@ -128,14 +131,16 @@ def workspace(device, B, K, V, dtype):
 
 
 def sd_verify(target, draft, drafts, out_tokens, num_accepted, temperature=None, seed=0,
-              p_at_draft=None, q_at_draft=None, err=None, stream=None, workspace_buf=None):
+              p_at_draft=None, q_at_draft=None, err=None, stream=None, workspace_buf=None,
+              request_base=0):
     """Verify K drafts per request (see include/sd.h).
 
     target: [B*(K+1), V] float32 probabilities or bfloat16 logits; draft: [B*K, V] same dtype;
     drafts: [B, K] int32; out_tokens: [B, K+1] int32; num_accepted: [B] int32;
     temperature: [B] float32 or None; p_at_draft / q_at_draft: [B, K] float32 or None;
     err: [1] int32 or None; workspace_buf: zeroed uint8 device tensor of at least
-    sd_verify_workspace_bytes bytes, or None for this device's shared one.
+    sd_verify_workspace_bytes bytes, or None for this device's shared one; request_base: the
+    global request index of local request 0 (a shard of a larger batch).
     """
     import torch
 
@@ -154,10 +159,18 @@ def sd_verify(target, draft, drafts, out_tokens, num_accepted, temperature=None,
     ws = workspace_buf if workspace_buf is not None else workspace(target.device, B, K, V, dtype)
     rc = load().sd_verify(B, K, V, dtype, _ptr(target), _row_stride(target), _ptr(draft),
                           _row_stride(draft), _ptr(drafts), _ptr(temperature), seed,
-                          _ptr(out_tokens), _ptr(num_accepted), _ptr(p_at_draft),
+                          request_base, _ptr(out_tokens), _ptr(num_accepted), _ptr(p_at_draft),
                           _ptr(q_at_draft), _ptr(ws), ws.numel(), _ptr(err),
                           _stream(target, stream))
     _check(rc, "sd_verify")
+
+
+def sd_verify_kernels(B, V, dtype, has_temperature):
+    """How many kernels one sd_verify call with these sizes launches on the current device."""
+    n = load().sd_verify_kernels(B, V, dtype, int(bool(has_temperature)))
+    if n < 0:
+        raise SDError(f"sd_verify_kernels: {load().sd_status_string(n).decode()}")
+    return n
 
 
 def sd_pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,

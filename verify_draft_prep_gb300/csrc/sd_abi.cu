@@ -8,12 +8,13 @@
 
 extern "C" {
 int sd_verify_launch(int, int, int, int, const void*, long, const void*, long, const int32_t*,
-                     const float*, uint64_t, int32_t*, int32_t*, float*, float*, void*, int32_t*,
-                     cudaStream_t);
+                     const float*, uint64_t, uint32_t, int32_t*, int32_t*, float*, float*, void*,
+                     int32_t*, cudaStream_t);
 size_t sd_verify_workspace_launch(int);
 int sd_verify_noalloc_launch(int, int, int, int, const void*, long, const void*, long,
-                             const int32_t*, const float*, uint64_t, int32_t*, int32_t*, float*,
-                             float*, int32_t*, cudaStream_t);
+                             const int32_t*, const float*, uint64_t, uint32_t, int32_t*, int32_t*,
+                             float*, float*, int32_t*, cudaStream_t);
+int sd_verify_kernel_count(int, int, int, int);
 int sd_prep_launch(int, int, const int32_t*, const int32_t*, const int32_t*, const int32_t*, int,
                    int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
                    int32_t*, int32_t*, int32_t*, int, const void*, long, int, const void*, void*,
@@ -72,13 +73,24 @@ size_t sd_verify_workspace_bytes(int B, int K, int V, int dtype) {
   return B > 0 ? sd_verify_workspace_launch(B) : 0;
 }
 
+int sd_verify_kernels(int B, int V, int dtype, int has_temperature) {
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || V < 1) return SD_E_SHAPE;
+  if (B == 0) return 0;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_verify_kernel_count(B, V, dtype, has_temperature);
+}
+
 int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft,
               long ld_d, const int32_t* drafts, const float* temperature, uint64_t seed,
-              int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
-              void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+              uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
+              float* p_at_draft, float* q_at_draft, void* workspace, size_t workspace_bytes,
+              int32_t* err, void* stream) {
   if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
   if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
   if ((long long)B * (K + 1) > 2147483647LL) return SD_E_SHAPE;
+  if ((unsigned long long)request_base + (unsigned long long)B > 4294967296ULL) return SD_E_SHAPE;
   if (B == 0) return SD_OK;
   if (!target || !draft || !drafts || !out_tokens || !num_accepted || !workspace) return SD_E_NULL;
   if (workspace_bytes < sd_verify_workspace_bytes(B, K, V, dtype)) return SD_E_SHAPE;
@@ -88,18 +100,19 @@ int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, con
   const int dev = check_device();
   if (dev != SD_OK) return dev;
   return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
-                          out_tokens, num_accepted, p_at_draft, q_at_draft, workspace, err,
-                          (cudaStream_t)stream);
+                          request_base, out_tokens, num_accepted, p_at_draft, q_at_draft,
+                          workspace, err, (cudaStream_t)stream);
 }
 
 int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target, long ld_t,
                       const void* draft, long ld_d, const int32_t* drafts,
-                      const float* temperature, uint64_t seed, int32_t* out_tokens,
-                      int32_t* num_accepted, float* p_at_draft, float* q_at_draft, int32_t* err,
-                      void* stream) {
+                      const float* temperature, uint64_t seed, uint32_t request_base,
+                      int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft,
+                      float* q_at_draft, int32_t* err, void* stream) {
   if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
   if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
   if (B > SD_VERIFY_NOALLOC_MAX_B) return SD_E_NOALLOC_LIMIT;
+  if ((unsigned long long)request_base + (unsigned long long)B > 4294967296ULL) return SD_E_SHAPE;
   if (B == 0) return SD_OK;
   if (!target || !draft || !drafts || !out_tokens || !num_accepted) return SD_E_NULL;
   const int esize = dtype == SD_F32_PROBS ? 4 : 2;
@@ -107,8 +120,8 @@ int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target, long l
   const int dev = check_device();
   if (dev != SD_OK) return dev;
   return sd_verify_noalloc_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature,
-                                  seed, out_tokens, num_accepted, p_at_draft, q_at_draft, err,
-                                  (cudaStream_t)stream);
+                                  seed, request_base, out_tokens, num_accepted, p_at_draft,
+                                  q_at_draft, err, (cudaStream_t)stream);
 }
 
 namespace {

@@ -59,6 +59,7 @@ struct VerifyParams {
   const int32_t* drafts;
   const float* temperature;
   PhiloxRoundKeys rk;
+  uint32_t rbase;  // request index of row 0 in the Philox counters (global index of a shard)
   int32_t* out_tokens;
   int32_t* num_accepted;
   float* p_at;
@@ -673,7 +674,7 @@ __device__ int accept_scan_warp(const VerifyParams& P, int r, float* Ps, float* 
     if (d >= 0 && (uint32_t)d < V) {
       Pv = __ldg(trow + d);
       Qv = __ldg(drow + d);
-      const double u = accept_uniform(P.rk, (uint32_t)r, (uint32_t)j);
+      const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
       acc = u * (double)Qv < (double)Pv;  // u*Q is exact in double
     } else {
       bad = true;
@@ -746,7 +747,7 @@ __device__ __noinline__ void finish_sampled(const VerifyParams& P, int r, int a,
   if (packed_key_bits(pk) == 0u && a < K) {
     // no positive residual key anywhere in the row: race on p of the same row, whole row
     F32Residual<false> src{prow, nullptr, V, vec};
-    pk = race_chunk(src, 0u, NU, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+    pk = race_chunk(src, 0u, NU, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
   }
   uint32_t b = 0;
   if (packed_key_bits(pk) == 0u) e |= SD_ERR_ZERO_ROW;
@@ -802,7 +803,7 @@ __device__ __noinline__ void finish_race(const VerifyParams& P, int r, int a, ui
   if (packed_key_bits(pk) == 0u && a < K) {
     // no positive residual key anywhere in the row: race on p of the same row, whole row
     F32Residual<false> src{prow, nullptr, V, P.vec != 0};
-    pk = race_chunk(src, 0u, NU, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+    pk = race_chunk(src, 0u, NU, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
   }
   if (threadIdx.x == 0) {
     uint32_t b = 0;
@@ -839,7 +840,7 @@ __device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Sme
     const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
     const float* qrow = a < K ? (const float*)P.draft + ((size_t)r * K + jr) * P.ld_d : nullptr;
     const F32ResidualAny src{prow, qrow, V, vec};
-    const uint64_t pk = race_chunk(src, lo, hi, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+    const uint64_t pk = race_chunk(src, lo, hi, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     uint64_t row_max;
     if (merge_slot(P.slots + r, pk, hi - lo, NU, sm, row_max)) finish_race(P, r, a, row_max, sm);
   }
@@ -942,10 +943,10 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
     uint64_t pk;
     if (a < K) {
       F32Residual<true> src{(const float*)trow(jr), (const float*)drow(jr), V, vec};
-      pk = race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+      pk = race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     } else {
       F32Residual<false> src{(const float*)trow(jr), nullptr, V, vec};
-      pk = race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm);
+      pk = race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     }
     uint64_t row_max;
     if (merge_slot(P.slots + r, pk, u1 - u0, NU, sm, row_max))
@@ -977,7 +978,7 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
                                                   sd.m),
                                         c)),
                        sd.s);
-        const double u = accept_uniform(P.rk, (uint32_t)r, (uint32_t)j);
+        const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
         accept = u * (double)Qv < (double)Pv;
       } else {
         e |= SD_ERR_TOKEN_RANGE;
@@ -992,11 +993,11 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
         Bf16Residual<true> src{t16 + (size_t)j * P.ld_t, d16 + (size_t)j * P.ld_d, st.m,
                                1.0f / st.s, sd.m, 1.0f / sd.s, c, V, vec};
         uint64_t pk = cluster_max_u64(
-            race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)j, sm), sm, phase, cl);
+            race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)j, sm), sm, phase, cl);
         if (packed_key_bits(pk) == 0u) {
           Bf16Residual<false> srcp{t16 + (size_t)j * P.ld_t, nullptr, st.m, 1.0f / st.s,
                                    0.0f, 0.0f, c, V, vec};
-          pk = cluster_max_u64(race_chunk(srcp, u0, u1, P.rk, (uint32_t)r, (uint32_t)j, sm),
+          pk = cluster_max_u64(race_chunk(srcp, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)j, sm),
                                sm, phase, cl);
         }
         if (packed_key_bits(pk) == 0u) {
@@ -1016,7 +1017,7 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
       Bf16Residual<false> src{t16 + (size_t)jr * P.ld_t, nullptr, st.m, 1.0f / st.s,
                               0.0f, 0.0f, c, V, vec};
       const uint64_t pk = cluster_max_u64(
-          race_chunk(src, u0, u1, P.rk, (uint32_t)r, (uint32_t)jr, sm), sm, phase, cl);
+          race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm), sm, phase, cl);
       if (packed_key_bits(pk) == 0u) {
         e |= SD_ERR_ZERO_ROW;
         b = 0;
@@ -1096,9 +1097,29 @@ int choose_cluster(int V, int epu) {
 
 }  // namespace
 
+// CTAs of the race phase for an all-sampled batch, or 0 when the batch stays in the one cluster
+// kernel. An all-sampled batch (temperature NULL) on large probability rows whose cluster grid
+// would span several waves takes the accept phase and then the race phase over a whole number of
+// CTAs per SM; smaller batches stay in the one cluster kernel (measured faster for them).
+static int race_grid(int B, int V, int dtype, bool has_temperature, int nc) {
+  if (dtype != SD_F32_PROBS || (V + 3) / 4 < 2048 || has_temperature) return 0;
+  if ((long)B * nc < 2L * sdk::kMinBlocks * sm_count()) return 0;
+  // a CTA's share spans at most B/g + 2 requests: g >= B/6 keeps that within 8
+  int g = sdk::kRaceMinBlocks * sm_count();
+  if (g < (B + 5) / 6) g = (B + 5) / 6;
+  return g;
+}
+
+extern "C" int sd_verify_kernel_count(int B, int V, int dtype, int has_temperature) {
+  if (B == 0) return 0;
+  const int epu = dtype == SD_F32_PROBS ? 4 : 8;
+  return race_grid(B, V, dtype, has_temperature != 0, choose_cluster(V, epu)) ? 2 : 1;
+}
+
 extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* target, long ld_t,
                                 const void* draft, long ld_d, const int32_t* drafts,
-                                const float* temperature, uint64_t seed, int32_t* out_tokens,
+                                const float* temperature, uint64_t seed, uint32_t request_base,
+                                int32_t* out_tokens,
                                 int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
                                 void* workspace, int32_t* err, cudaStream_t stream) {
   const int esize = dtype == SD_F32_PROBS ? 4 : 2;
@@ -1114,6 +1135,7 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.drafts = drafts;
   P.temperature = temperature;
   P.rk = sdk::philox_round_keys(seed);
+  P.rbase = request_base;
   P.out_tokens = out_tokens;
   P.num_accepted = num_accepted;
   P.p_at = p_at_draft;
@@ -1126,14 +1148,7 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   // An all-sampled batch (temperature NULL) on large probability rows whose cluster grid would
   // span several waves takes the accept phase and then the race phase over a whole number of
   // CTAs per SM; smaller batches stay in the one cluster kernel (measured faster for them).
-  P.race_blocks = 0;
-  if (dtype == SD_F32_PROBS && (V + 3) / 4 >= 2048 && temperature == nullptr &&
-      (long)B * P.nc >= 2L * sdk::kMinBlocks * sm_count()) {
-    // a CTA's share spans at most B/g + 2 requests: g >= B/6 keeps that within 8
-    int g = sdk::kRaceMinBlocks * sm_count();
-    if (g < (B + 5) / 6) g = (B + 5) / 6;
-    P.race_blocks = g;
-  }
+  P.race_blocks = race_grid(B, V, dtype, temperature != nullptr, P.nc);
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
   if (B == 0) return SD_OK;
@@ -1206,7 +1221,8 @@ std::atomic<void*> g_noalloc_addr[kNoallocMaxDevices];
 extern "C" int sd_verify_noalloc_launch(int B, int K, int V, int dtype, const void* target,
                                         long ld_t, const void* draft, long ld_d,
                                         const int32_t* drafts, const float* temperature,
-                                        uint64_t seed, int32_t* out_tokens, int32_t* num_accepted,
+                                        uint64_t seed, uint32_t request_base,
+                                        int32_t* out_tokens, int32_t* num_accepted,
                                         float* p_at_draft, float* q_at_draft, int32_t* err,
                                         cudaStream_t stream) {
   int dev = 0;
@@ -1223,5 +1239,6 @@ extern "C" int sd_verify_noalloc_launch(int B, int K, int V, int dtype, const vo
   if (cudaMemsetAsync(slots, 0, (size_t)B * sizeof(sdk::RaceSlot), stream) != cudaSuccess)
     return SD_E_LAUNCH;
   return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
-                          out_tokens, num_accepted, p_at_draft, q_at_draft, slots, err, stream);
+                          request_base, out_tokens, num_accepted, p_at_draft, q_at_draft, slots,
+                          err, stream);
 }
