@@ -128,11 +128,10 @@ SD_API size_t sd_verify_workspace_bytes(int B, int K, int V, int dtype);
 
 /*
  * Number of kernels one sd_verify (or sd_verify_noalloc) call with these sizes launches on the
- * current device: 0 for B == 0; 2 when every request samples (has_temperature == 0) on large
- * probability rows and the batch fills the GPU several times (an accept kernel, then a race
- * kernel balanced over all SMs); 1 otherwise. A planning query for callers that count launches
- * (a CUDA-graph budget, a profiler filter); it launches nothing. Returns a negative status for
- * an unknown dtype or B < 0, V < 1.
+ * current device: 0 for B == 0, else 1 (the cluster kernel, or for an all-sampled batch on large
+ * probability rows the race kernel that balances the batch over every SM). A planning query for
+ * callers that count launches (a CUDA-graph budget, a profiler filter); it launches nothing.
+ * Returns a negative status for an unknown dtype or B < 0, V < 1.
  */
 SD_API int sd_verify_kernels(int B, int V, int dtype, int has_temperature);
 

@@ -119,6 +119,14 @@ __device__ __forceinline__ float fast_lg2(float x) {
   return y;
 }
 
+// 2^x by the hardware approximation with flush-to-zero: results below 2^-126 become 0. The
+// softmax terms that flush are more than 2^126 times smaller than the row's largest term.
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float fast_rcp(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

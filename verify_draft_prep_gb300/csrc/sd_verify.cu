@@ -27,6 +27,7 @@
 #include <float.h>
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 #include <type_traits>
 
@@ -41,6 +42,10 @@ constexpr int kMinBlocks = 4;  // resident CTAs per SM the cluster kernel's regi
 constexpr int kRaceMinBlocks = 4;  // the same for race_kernel (its loop keeps 3 units in flight)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
 constexpr int kCandCap = 32;            // candidate units evaluated lane-parallel per CTA
+constexpr int kMaxSeg = NT / 32;        // requests one race-kernel CTA may touch (a warp each)
+// A unit whose bound r_max * R(w_max) * kSkip stays below the CTA's running best is skipped (see
+// race_take): (1 + kBand) for the filter's band, 2^-9 for the approximations inside the bound.
+constexpr float kSkip = (1.0f + kBand) * (1.0f + 0x1p-9f);
 
 // Per-request merge slot in the caller's workspace: the packed (key, ~x) maximum over the
 // request's CTAs and the number of CTAs that have merged. The last CTA resets both to zero.
@@ -159,6 +164,12 @@ struct F32Residual {
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[i] = HAS_Q ? __fsub_rn(raw.p[i], raw.q[i]) : raw.p[i];
   }
+  // an upper bound of the unit's residuals (here their maximum)
+  __device__ __forceinline__ float residual_bound(const Raw& raw) const {
+    float r[4];
+    residual(raw, r);
+    return fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+  }
   __device__ __forceinline__ float at(uint32_t x) const {
     return HAS_Q ? __fsub_rn(__ldg(p + x), __ldg(q + x)) : __ldg(p + x);
   }
@@ -197,6 +208,11 @@ struct F32ResidualAny {
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[i] = __fsub_rn(raw.p[i], raw.q[i]);
   }
+  __device__ __forceinline__ float residual_bound(const Raw& raw) const {
+    float r[4];
+    residual(raw, r);
+    return fmaxf(fmaxf(r[0], r[1]), fmaxf(r[2], r[3]));
+  }
   __device__ __forceinline__ float at(uint32_t x) const {
     return q ? __fsub_rn(__ldg(p + x), __ldg(q + x)) : __ldg(p + x);
   }
@@ -205,7 +221,7 @@ struct F32ResidualAny {
 // p(x) = exp2((l - M) * c) / S with c = log2(e) / T, written with explicit roundings so that the
 // streamed pass and the scalar re-evaluation of a candidate give the same bits.
 __device__ __forceinline__ float logit_prob(float l, float M, float c, float invS) {
-  return __fmul_rn(exp2f(__fmul_rn(__fsub_rn(l, M), c)), invS);
+  return __fmul_rn(fast_ex2(__fmul_rn(__fsub_rn(l, M), c)), invS);
 }
 
 template <bool HAS_Q>
@@ -248,6 +264,17 @@ struct Bf16Residual {
       r[i] = HAS_Q ? __fsub_rn(pv, logit_prob(bf16_at(raw.d, i), Md, c, invSd)) : pv;
     }
   }
+  // An upper bound of the unit's residuals without their exponentials: r(x) <= p(x) (q >= 0),
+  // and p at the unit's largest target logit bounds every p(x) of the unit up to the hardware
+  // exponential's non-monotonicity (far below the 2^-9 allowed for in kSkip).
+  __device__ __forceinline__ float residual_bound(const Raw& raw) const {
+    uint32_t m01, m23, m;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m01) : "r"(raw.t.x), "r"(raw.t.y));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m23) : "r"(raw.t.z), "r"(raw.t.w));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
+    const float lmax = fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    return logit_prob(lmax, Mt, c, invSt);
+  }
   __device__ __forceinline__ float at(uint32_t x) const {
     const float pv = logit_prob(bf16_bits_to_float(__ldg(t + x)), Mt, c, invSt);
     return HAS_Q ? __fsub_rn(pv, logit_prob(bf16_bits_to_float(__ldg(d + x)), Md, c, invSd)) : pv;
@@ -268,6 +295,7 @@ struct Smem {
   int ncand;
   uint32_t cand[kCandCap];
   int last;
+  uint32_t tau;  // race_take's running best of the current race_chunk call (fp32 bits)
 };
 
 // Cluster-wide maximum of a CTA-uniform value. Every CTA of the cluster calls it the same
@@ -304,9 +332,18 @@ __device__ __forceinline__ uint64_t exact_key(float r, uint32_t w, uint32_t x) {
   return pack_key(__float_as_uint(key), x);
 }
 
-// Largest approximate key of one unit (0 when no residual is positive).
 template <int EPU>
-__device__ __forceinline__ float unit_max_alpha(const float (&r)[EPU], const uint4 (&w)[EPU / 4]) {
+__device__ __forceinline__ uint32_t unit_wmax(const uint4 (&w)[EPU / 4]) {
+  uint32_t wmax = 0;
+#pragma unroll
+  for (int h = 0; h < EPU / 4; ++h) wmax = max(wmax, max(max(w[h].x, w[h].y), max(w[h].z, w[h].w)));
+  return wmax;
+}
+
+// Largest approximate key of one unit (0 when no residual is positive); wmax = unit_wmax(w).
+template <int EPU>
+__device__ __forceinline__ float unit_max_alpha(const float (&r)[EPU], const uint4 (&w)[EPU / 4],
+                                                uint32_t wmax) {
   float R[EPU];
 #pragma unroll
   for (int h = 0; h < EPU / 4; ++h) {
@@ -315,9 +352,6 @@ __device__ __forceinline__ float unit_max_alpha(const float (&r)[EPU], const uin
     R[4 * h + 2] = race_R_main(w[h].z);
     R[4 * h + 3] = race_R_main(w[h].w);
   }
-  uint32_t wmax = 0;
-#pragma unroll
-  for (int h = 0; h < EPU / 4; ++h) wmax = max(wmax, max(max(w[h].x, w[h].y), max(w[h].z, w[h].w)));
   if (wmax >= kNearOne) {  // one word in 8192: redo those few near v = 1
 #pragma unroll
     for (int e = 0; e < EPU; ++e) {
@@ -358,15 +392,25 @@ __device__ __noinline__ void exact_unit(const Src& src, uint32_t u, const Philox
   }
 }
 
+// One unit of the streaming pass. *tau is the largest unit maximum any thread of the CTA has
+// posted for this row so far (0 at the start of each race_chunk call); it and a1 are maxima of
+// computed units, so neither exceeds A. A unit whose bound r_max * R(w_max) * kSkip (R rises with
+// the word, so R(w_max) bounds R(w_x) of the unit up to the approximation error) stays below
+// max(a1, *tau) has m * (1 + kBand) < A: it cannot be a candidate, and skipping it changes
+// neither A nor a thread's candidate units; its keys are not computed.
 template <class Src>
 __device__ __forceinline__ void race_take(const Src& src, const typename Src::Raw& raw,
                                           const uint4 (&w)[Src::EPU / 4], uint32_t u, float& a1,
-                                          float& a2, uint32_t& best_u) {
+                                          float& a2, uint32_t& best_u, uint32_t* tau) {
+  const uint32_t wmax = unit_wmax<Src::EPU>(w);
+  const float thr = fmaxf(a1, __uint_as_float(*(volatile uint32_t*)tau));
+  if (src.residual_bound(raw) * race_R(wmax) * kSkip < thr) return;
   float r[Src::EPU];
   src.residual(raw, r);
-  const float m = unit_max_alpha<Src::EPU>(r, w);
+  const float m = unit_max_alpha<Src::EPU>(r, w, wmax);
   a2 = fmaxf(a2, fminf(m, a1));
   best_u = m > a1 ? u : best_u;
+  if (m > thr) atomicMax(tau, __float_as_uint(m));  // keys are >= 0: ordered as integers
   a1 = fmaxf(a1, m);
 }
 
@@ -393,7 +437,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
         const uint32_t u = ub + k * NT;
         uint4 w[EPU / 4];
         unit_words<Src>(rk, u, rid, j, w);
-        race_take(src, raw[k], w, u, a1, a2, best_u);
+        race_take(src, raw[k], w, u, a1, a2, best_u, &sm.tau);
         src.fetch_fast(u + UNR * NT, raw[k]);
       }
     }
@@ -402,7 +446,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
       const uint32_t u = ub + k * NT;
       uint4 w[EPU / 4];
       unit_words<Src>(rk, u, rid, j, w);
-      race_take(src, raw[k], w, u, a1, a2, best_u);
+      race_take(src, raw[k], w, u, a1, a2, best_u, &sm.tau);
     }
     ub += UNR * NT;
   }
@@ -411,10 +455,11 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
     src.fetch(ub, raw);
     uint4 w[EPU / 4];
     unit_words<Src>(rk, ub, rid, j, w);
-    race_take(src, raw, w, ub, a1, a2, best_u);
+    race_take(src, raw, w, ub, a1, a2, best_u, &sm.tau);
   }
   if (threadIdx.x == 0) sm.ncand = 0;
   const float A = __uint_as_float((uint32_t)block_max_u64<NT>(__float_as_uint(a1), sm.red));
+  if (threadIdx.x == 0) sm.tau = 0u;  // every thread has left the streaming pass
   uint64_t best = 0ull;
   if (A > 0.0f) {
     // A CTA maximum below about 2^-100 in key units: fp32 keys are near the subnormal range
@@ -436,7 +481,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
           src.residual(raw, r);
           uint4 w[EPU / 4];
           unit_words<Src>(rk, u, rid, j, w);
-          take = unit_max_alpha<EPU>(r, w) * (1.0f + kBand) >= A;
+          take = unit_max_alpha<EPU>(r, w, unit_wmax<EPU>(w)) * (1.0f + kBand) >= A;
         }
         if (take) exact_unit(src, u, rk, rid, j, best);
       }
@@ -531,8 +576,8 @@ struct MaxSum {
 __device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b, float c) {
   const float m = fmaxf(a.m, b.m);
   if (m == -INFINITY) return MaxSum{m, 0.0f};
-  const float sa = a.m == -INFINITY ? 0.0f : a.s * exp2f((a.m - m) * c);
-  const float sb = b.m == -INFINITY ? 0.0f : b.s * exp2f((b.m - m) * c);
+  const float sa = a.m == -INFINITY ? 0.0f : a.s * fast_ex2((a.m - m) * c);
+  const float sb = b.m == -INFINITY ? 0.0f : b.s * fast_ex2((b.m - m) * c);
   return MaxSum{m, sa + sb};
 }
 
@@ -545,7 +590,7 @@ __device__ __forceinline__ void absorb_unit(MaxSum& st, float& comp, const uint4
   for (int i = 1; i < 8; ++i) um = fmaxf(um, v[i]);
   if (um > st.m) {
     if (st.m != -INFINITY) {
-      const float f = exp2f((st.m - um) * c);
+      const float f = fast_ex2((st.m - um) * c);
       st.s *= f;
       comp *= f;
     }
@@ -554,7 +599,7 @@ __device__ __forceinline__ void absorb_unit(MaxSum& st, float& comp, const uint4
   if (st.m == -INFINITY) return;
   float e[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) e[i] = exp2f((v[i] - st.m) * c);
+  for (int i = 0; i < 8; ++i) e[i] = fast_ex2((v[i] - st.m) * c);
   const float part = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
   // compensated running sum
   const float y = part - comp;
@@ -759,69 +804,21 @@ __device__ __noinline__ void finish_sampled(const VerifyParams& P, int r, int a,
   write_request(P, r, a, b, e, Ps, Qs);
 }
 
-// Accept phase of an all-sampled batch: one warp per request. Writes num_accepted, the accepted
-// drafts and the -1 padding of out_tokens (the final token's place is left to the race phase),
-// P/Q at the drafts and the out-of-range error bit.
-__global__ void __launch_bounds__(NT) accept_kernel(const __grid_constant__ VerifyParams P) {
-  __shared__ float Ps[NT / 32][SD_K_MAX], Qs[NT / 32][SD_K_MAX];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (NT / 32) + warp;
-  if (r >= P.B) return;  // warp-uniform
-  const int K = P.K;
-  if (lane < SD_K_MAX) {
-    Ps[warp][lane] = -1.0f;
-    Qs[warp][lane] = -1.0f;
-  }
-  __syncwarp();
-  int bad;
-  const int a = accept_scan_warp(P, r, Ps[warp], Qs[warp], &bad);
-  __syncwarp();
-  if (lane <= K && lane != a) {
-    P.out_tokens[(size_t)r * (K + 1) + lane] =
-        lane < a ? __ldg(P.drafts + (size_t)r * K + lane) : -1;
-  }
-  if (lane < K) {
-    if (P.p_at) P.p_at[(size_t)r * K + lane] = Ps[warp][lane];
-    if (P.q_at) P.q_at[(size_t)r * K + lane] = Qs[warp][lane];
-  }
-  if (lane == 0) {
-    P.num_accepted[r] = a;
-    raise_err(P.err, bad);
-  }
-}
+// The race kernel: an all-sampled batch in one launch. The requests' race rows are laid end to
+// end (unit u of request r at position r*NU + u) and that line is split evenly over race_blocks
+// CTAs (a whole number per SM). Every unit costs the same Philox and filter arithmetic, and that,
+// more than the one or two rows a unit reads, sets a CTA's time (measured: balancing by bytes
+// instead was slower), so every SM gets the same number of units. The split does not depend on
+// which row a request races on, so each CTA first runs the accept scan of the few requests its
+// share touches (one warp each; CTAs sharing a request compute the same result), then races over
+// its segments; the CTA that completes a request's row writes all of that request's outputs.
+struct AcceptState {
+  float P[kMaxSeg][SD_K_MAX], Q[kMaxSeg][SD_K_MAX];
+  int a[kMaxSeg], e[kMaxSeg];
+};
 
-// The CTA that completed request r's race row (race phase): fallback, the final token, slot reset.
-__device__ __noinline__ void finish_race(const VerifyParams& P, int r, int a, uint64_t pk,
-                                         Smem& sm) {
-  const int K = P.K;
-  const uint32_t V = (uint32_t)P.V;
-  const uint32_t NU = (V + 3u) / 4u;
-  const int jr = a < K ? a : K;
-  const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
-  if (packed_key_bits(pk) == 0u && a < K) {
-    // no positive residual key anywhere in the row: race on p of the same row, whole row
-    F32Residual<false> src{prow, nullptr, V, P.vec != 0};
-    pk = race_chunk(src, 0u, NU, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
-  }
-  if (threadIdx.x == 0) {
-    uint32_t b = 0;
-    if (packed_key_bits(pk) == 0u) raise_err(P.err, SD_ERR_ZERO_ROW);
-    else b = packed_index(pk);
-    P.out_tokens[(size_t)r * (K + 1) + a] = (int32_t)b;
-    P.slots[r].best = 0ull;
-    P.slots[r].count = 0u;
-  }
-}
-
-// Race phase of an all-sampled batch: the requests' race rows laid end to end (unit u of request
-// r at position r*NU + u) and that line split evenly over race_blocks CTAs (a whole number per
-// SM). Every unit costs the same Philox and filter arithmetic, and that, more than the one or
-// two rows a unit reads, sets a CTA's time (measured: balancing by bytes instead was slower), so
-// every SM gets the same number of units. A CTA covers one or a few request segments; the CTA
-// that completes a row finishes its request.
-__device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Smem& sm) {
+__device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Smem& sm,
+                                          AcceptState& as) {
   const int K = P.K;
   const uint32_t V = (uint32_t)P.V;
   const uint32_t NU = (V + 3u) / 4u;
@@ -831,18 +828,36 @@ __device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Sme
   const unsigned long long w1 = W * (c + 1) / (unsigned)P.race_blocks;
   if (w1 <= w0) return;  // CTA-uniform
   const int r0 = (int)(w0 / NU), r1 = (int)((w1 - 1) / NU);  // at most kMaxSeg requests
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp <= r1 - r0) {  // warp-uniform
+    if (lane < SD_K_MAX) {
+      as.P[warp][lane] = -1.0f;
+      as.Q[warp][lane] = -1.0f;
+    }
+    __syncwarp();
+    int bad;
+    const int a = accept_scan_warp(P, r0 + warp, as.P[warp], as.Q[warp], &bad);
+    if (lane == 0) {
+      as.a[warp] = a;
+      as.e[warp] = bad;
+    }
+  }
+  if (threadIdx.x == 0) sm.tau = 0u;
+  __syncthreads();
   for (int r = r0; r <= r1; ++r) {
     const unsigned long long base = (unsigned long long)r * NU;
     const uint32_t lo = (uint32_t)(max(w0, base) - base);
     const uint32_t hi = (uint32_t)(min(w1, base + NU) - base);
-    const int a = P.num_accepted[r];
+    const int i = r - r0;
+    const int a = as.a[i];
     const int jr = a < K ? a : K;
     const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
     const float* qrow = a < K ? (const float*)P.draft + ((size_t)r * K + jr) * P.ld_d : nullptr;
     const F32ResidualAny src{prow, qrow, V, vec};
     const uint64_t pk = race_chunk(src, lo, hi, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     uint64_t row_max;
-    if (merge_slot(P.slots + r, pk, hi - lo, NU, sm, row_max)) finish_race(P, r, a, row_max, sm);
+    if (merge_slot(P.slots + r, pk, hi - lo, NU, sm, row_max))
+      finish_sampled(P, r, a, as.e[i], row_max, as.P[i], as.Q[i], sm);
   }
 }
 
@@ -890,6 +905,7 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
     sm.P[threadIdx.x] = -1.0f;
     sm.Q[threadIdx.x] = -1.0f;
   }
+  if (threadIdx.x == 0) sm.tau = 0u;
   __syncthreads();
 
   if (greedy) {
@@ -1058,8 +1074,9 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
 __global__ void __launch_bounds__(NT, kRaceMinBlocks)
     race_kernel(const __grid_constant__ VerifyParams P) {
   __shared__ Smem sm;
+  __shared__ AcceptState as;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  race_role(P, blockIdx.x, sm);
+  race_role(P, blockIdx.x, sm, as);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
@@ -1097,23 +1114,24 @@ int choose_cluster(int V, int epu) {
 
 }  // namespace
 
-// CTAs of the race phase for an all-sampled batch, or 0 when the batch stays in the one cluster
-// kernel. An all-sampled batch (temperature NULL) on large probability rows whose cluster grid
-// would span several waves takes the accept phase and then the race phase over a whole number of
-// CTAs per SM; smaller batches stay in the one cluster kernel (measured faster for them).
+// CTAs of the race kernel for an all-sampled batch (temperature NULL) on probability rows of at
+// least 8192 entries whose cluster grid would span two waves or more (a whole number of CTAs per
+// SM), or 0 for the cluster kernel.
 static int race_grid(int B, int V, int dtype, bool has_temperature, int nc) {
   if (dtype != SD_F32_PROBS || (V + 3) / 4 < 2048 || has_temperature) return 0;
-  if ((long)B * nc < 2L * sdk::kMinBlocks * sm_count()) return 0;
-  // a CTA's share spans at most B/g + 2 requests: g >= B/6 keeps that within 8
-  int g = sdk::kRaceMinBlocks * sm_count();
+  const int sms = sm_count();
+  if ((long)B * nc < 2L * sdk::kMinBlocks * sms) return 0;  // measured faster in clusters
+  long g = (long)sdk::kRaceMinBlocks * sms;
+  // a CTA's share spans at most B/g + 2 requests: g >= B/6 keeps that within kMaxSeg
   if (g < (B + 5) / 6) g = (B + 5) / 6;
-  return g;
+  return (int)g;
 }
 
 extern "C" int sd_verify_kernel_count(int B, int V, int dtype, int has_temperature) {
-  if (B == 0) return 0;
-  const int epu = dtype == SD_F32_PROBS ? 4 : 8;
-  return race_grid(B, V, dtype, has_temperature != 0, choose_cluster(V, epu)) ? 2 : 1;
+  (void)V;
+  (void)dtype;
+  (void)has_temperature;
+  return B == 0 ? 0 : 1;  // the cluster kernel or the race kernel
 }
 
 extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* target, long ld_t,
@@ -1145,9 +1163,7 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.cl = choose_cluster(V, epu);
   P.nc = P.cl;  // CTAs per request in the cluster role
   P.cluster_blocks = B * P.nc;
-  // An all-sampled batch (temperature NULL) on large probability rows whose cluster grid would
-  // span several waves takes the accept phase and then the race phase over a whole number of
-  // CTAs per SM; smaller batches stay in the one cluster kernel (measured faster for them).
+  // an all-sampled batch on large probability rows takes the race kernel instead (race_grid)
   P.race_blocks = race_grid(B, V, dtype, temperature != nullptr, P.nc);
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
@@ -1177,20 +1193,8 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
     return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
   }
   {
-    // every request sampled on probability rows: the accept phase, then the race phase balanced
-    // by bytes over the whole GPU (both programmatic dependents of what precedes them)
-    cudaLaunchConfig_t acfg = {};
-    acfg.gridDim = dim3((unsigned)((B + sdk::NT / 32 - 1) / (sdk::NT / 32)), 1, 1);
-    acfg.blockDim = dim3(sdk::NT, 1, 1);
-    acfg.stream = stream;
-    cudaLaunchAttribute aattr[1];
-    aattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    aattr[0].val.programmaticStreamSerializationAllowed = 1;
-    acfg.attrs = aattr;
-    acfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&acfg, sdk::accept_kernel, P) != cudaSuccess) return SD_E_LAUNCH;
-  }
-  {
+    // every request sampled on probability rows: accept scans and the race, balanced over every
+    // SM (a programmatic dependent of what precedes it)
     cudaLaunchConfig_t rcfg = {};
     rcfg.gridDim = dim3((unsigned)P.race_blocks, 1, 1);
     rcfg.blockDim = dim3(sdk::NT, 1, 1);
