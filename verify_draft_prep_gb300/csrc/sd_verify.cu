@@ -37,6 +37,7 @@ namespace sdk {
 
 constexpr int NT = 256;        // threads per CTA
 constexpr int UNROLL = 4;      // 16-byte units in flight per thread (greedy rows, statistics)
+constexpr int kArgmaxUnroll = 8;  // the same for greedy argmax rows (loads only: more in flight)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
 constexpr int kMinBlocks = 4;  // resident CTAs per SM the cluster kernel's registers allow
 constexpr int kRaceMinBlocks = 4;  // the same for race_kernel (its loop keeps 3 units in flight)
@@ -537,20 +538,20 @@ __device__ uint64_t argmax_chunk(const void* row, uint32_t V, bool vec, uint32_t
     }
   };
   auto load = [&](uint32_t u) { return ld_stream_u4((const char*)row + (size_t)u * 16u); };
-  if (ub + (UNROLL - 1) * NT < uf) {  // unchecked 128-bit loads, UNROLL units always in flight
-    uint4 v[UNROLL];
+  if (ub + (kArgmaxUnroll - 1) * NT < uf) {  // unchecked 128-bit loads, kArgmaxUnroll units always in flight
+    uint4 v[kArgmaxUnroll];
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) v[k] = load(ub + k * NT);
-    for (; ub + (2 * UNROLL - 1) * NT < uf; ub += UNROLL * NT) {
+    for (int k = 0; k < kArgmaxUnroll; ++k) v[k] = load(ub + k * NT);
+    for (; ub + (2 * kArgmaxUnroll - 1) * NT < uf; ub += kArgmaxUnroll * NT) {
 #pragma unroll
-      for (int k = 0; k < UNROLL; ++k) {
+      for (int k = 0; k < kArgmaxUnroll; ++k) {
         take(v[k], ub + k * NT);
-        v[k] = load(ub + (k + UNROLL) * NT);
+        v[k] = load(ub + (k + kArgmaxUnroll) * NT);
       }
     }
 #pragma unroll
-    for (int k = 0; k < UNROLL; ++k) take(v[k], ub + k * NT);
-    ub += UNROLL * NT;
+    for (int k = 0; k < kArgmaxUnroll; ++k) take(v[k], ub + k * NT);
+    ub += kArgmaxUnroll * NT;
   }
   for (; ub < u1; ub += NT) {  // the rest, bounds-checked
     if (DT == SD_F32_PROBS) {
@@ -1162,9 +1163,17 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.err = err;
   P.cl = choose_cluster(V, epu);
   P.nc = P.cl;  // CTAs per request in the cluster role
-  P.cluster_blocks = B * P.nc;
-  // an all-sampled batch on large probability rows takes the race kernel instead (race_grid)
   P.race_blocks = race_grid(B, V, dtype, temperature != nullptr, P.nc);
+  if (P.race_blocks == 0 && dtype == SD_F32_PROBS && temperature == nullptr) {
+    // every request samples: its CTAs exchange nothing through shared memory, so no cluster is
+    // needed, and each row splits over as many CTAs as fill one wave of kMinBlocks per SM
+    const int nu = (V + 3) / 4;
+    int nc = sdk::kMinBlocks * sm_count() / std::max(B, 1);
+    nc = std::min(nc, std::max(1, nu / (2 * sdk::NT)));
+    P.cl = 1;
+    P.nc = std::max(nc, 1);
+  }
+  P.cluster_blocks = B * P.nc;  // (unused when the race kernel takes the batch)
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
   if (B == 0) return SD_OK;
