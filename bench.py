@@ -35,7 +35,14 @@ L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the verify kernel, from one ncu
 # capture, keyed by workload and by the hash of the kernel source it was taken on (the number is
 # reported only while the source is unchanged).
-MEASURED_TRAFFIC = {}
+# Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
+# traffic grows in proportion to the requests).
+MEASURED_TRAFFIC = {
+    ("b64", "063107533b338996"): (82.450944e6, "ncu --set full, one launch of the full batch"),
+    ("b256mix", "063107533b338996"): (401.228288e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "063107533b338996"): (785.44e6, "ncu --set full at B=160, scaled x3.2"),
+    ("b1024lg", "063107533b338996"): (3055.43e6, "ncu --set full at B=96, scaled x1024/96"),
+}
 
 
 def _src_hash():
@@ -111,7 +118,15 @@ class ClockSampler:
 
 
 def algorithmic_bytes(w, a):
-    """Bytes the method must move per step, from the accepted counts a (numpy [B])."""
+    """Bytes the method must move per step, from the accepted counts a (numpy [B]): verify (the
+    roofline's model), expand, gather, and verify counting only the rows the kernel must read.
+
+    Probability rows use the minimum-bytes model: the scalar gathers of the accept scan plus one p
+    and one q row at the first rejection (only p when every draft is accepted), or the a_r + 1
+    rows a greedy request scans. Logit rows use the full-row model (every target and draft row of
+    the request, 2K + 1 rows), the roofline stated for the fused-softmax variant; the kernel
+    itself reads rows lazily (rows 0..a_r of both, and never the rows after the first
+    rejection), which the fourth figure counts."""
     import torch
 
     B, K, V, H = w.B, w.K, w.V, w.H
@@ -123,22 +138,24 @@ def algorithmic_bytes(w, a):
     if w.kind == "probs":
         rows = np.where(greedy, a + 1, np.where(a < K, 2, 1))
         gathers = np.where(greedy, 0, 2 * 32 * np.minimum(a + 1, K))
+        verify = verify_read = int((rows * esz * V + gathers + scalars).sum())
     else:
-        rows = np.where(greedy, a + 1, (a + 1) + np.minimum(a + 1, K))
-        gathers = np.zeros_like(a)
-    verify = int((rows * esz * V + gathers + scalars).sum())
+        verify = int(B * ((2 * K + 1) * esz * V + scalars))
+        rows_read = np.where(greedy, a + 1, (a + 1) + np.minimum(a + 1, K))
+        verify_read = int((rows_read * esz * V + scalars).sum())
     blocks = (2 * K) // w.block_size + 2
     expand = int((4 * (K + 4) + 4 * blocks + (a + K) * 17 + (K + 1) + 4 * K).sum())
     gather = int(((a + 1) * 2 * H + (a + K) * 2 * H).sum()) + 2 * H
     del torch
-    return verify, expand, gather
+    return verify, expand, gather, verify_read
 
 
-def make_sets(cfg_name, nsets, device, rank):
+def make_sets(cfg_name, nsets, device, rank, batch=None):
     import workloads
 
     idx = [c["name"] for c in workloads.CONFIGS].index(cfg_name)
-    return [workloads.make(idx, device=device, gen_seed=1000 + idx + 101 * s + 7919 * rank)
+    return [workloads.make(idx, device=device, gen_seed=1000 + idx + 101 * s + 7919 * rank,
+                           B=batch)
             for s in range(nsets)]
 
 
@@ -215,7 +232,7 @@ def time_graph(fn, sets, outs, stream, K):
     return a.elapsed_time(b) / K
 
 
-def run_cpu_baseline(w_host, budget_s=12.0):
+def run_cpu_baseline(w_host, budget_s=10.0):
     """Time the oracle (as it stands) on all host cores on one input set: requests/s."""
     import oracle
 
@@ -236,7 +253,7 @@ def run_cpu_baseline(w_host, budget_s=12.0):
                              w_host["h_shared"])
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
+        if el >= budget_s or reps >= 5000:
             break
     return {"value": B * reps / el, "unit": "requests/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} passes over all {B} requests of one input set "
@@ -271,6 +288,9 @@ def main():
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: auto)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: the config's shapes with this many requests (0: as "
+                         "configured); a line with a reduced batch is not the config's number")
     ap.add_argument("--step-events", action="store_true",
                     help="record an event at every step boundary (per-step times; the event "
                          "nodes break the programmatic launch edge between steps)")
@@ -302,9 +322,10 @@ def main():
     from verify_draft_prep_gb300 import shard
 
     cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
-    w0 = workloads.make(args.config, device=device, gen_seed=1000 + 7919 * rank)
+    batch = args.batch or None
+    w0 = workloads.make(args.config, device=device, gen_seed=1000 + 7919 * rank, B=batch)
     nsets = args.sets or (4 if cfg["B"] * cfg["V"] < 64 * 201088 * 2 else 2)
-    sets = [w0] + make_sets(args.config, nsets - 1, device, rank + 1)
+    sets = [w0] + make_sets(args.config, nsets - 1, device, rank + 1, batch)
     outs = [alloc_outputs(w, device) for w in sets]
     for w in sets:
         temperatures(w)  # decided before any graph capture (it reads the device)
@@ -321,7 +342,7 @@ def main():
     per_set = []
     for w, o in zip(sets, outs):
         a = o["num_accepted"].cpu().numpy()
-        per_set.append(algorithmic_bytes(w, a) + (a,))
+        per_set.append(algorithmic_bytes(w, a)[:3] + (a, algorithmic_bytes(w, a)[3]))
     errs = [int(o["err"].item()) for o in outs]
 
     # the timed steps are replayed from CUDA graphs of up to CHUNK steps (a graph of K % CHUNK
@@ -388,9 +409,12 @@ def main():
     value = shard.whole_job_rate(B * K, world, total_ms)
     bytes_v = float(np.mean([per_set[s % nsets][0] for s in range(CHUNK)]))
     bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(CHUNK)]))
+    bytes_read = float(np.mean([per_set[s % nsets][4] for s in range(CHUNK)]))
     peak, peak_kind = _peaks()
     achieved = bytes_v / (avg_v * 1e-3) / 1e9
-    traffic = MEASURED_TRAFFIC.get((args.config, _src_hash()))
+    traffic, traffic_note = (None, "no capture of the current kernel source")
+    if not args.batch and (args.config, _src_hash()) in MEASURED_TRAFFIC:
+        traffic, traffic_note = MEASURED_TRAFFIC[(args.config, _src_hash())]
 
     # end to end through the public API: pinned host inputs -> device, step, results -> host
     e2e = run_e2e(sd, sets[0], device, args.e2e_steps)
@@ -417,7 +441,9 @@ def main():
             "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32"
             if cfg["kind"] == "probs" else "bf16", "data": "synthetic",
-            "config": {"workload": workloads.config_label(cfg), "B": B, "K": sets[0].K,
+            "config": {"workload": workloads.config_label(cfg) + (
+                f" [reduced to B={B} for profiling]" if args.batch else ""), "B": B,
+                       "K": sets[0].K,
                        "V": sets[0].V, "H": sets[0].H,
                        "l2": f"{nsets} rotating input sets (rows of all sets "
                              f"{nsets * sets[0].target.numel() * sets[0].target.element_size() / 1e9:.1f} GB"
@@ -428,8 +454,14 @@ def main():
                        "parallelism": f"dp{world}: request shards of {B} per GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
+                         "traffic_source": traffic_note,
                          "kernel": "sd_verify", "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": bytes_v,
+                         "bytes_model": "minimum bytes (scalar gathers + one p and one q row "
+                                        "per sampled request, a_r + 1 rows per greedy one)"
+                         if cfg["kind"] == "probs" else
+                         "full rows (2K + 1 logit rows per request)",
+                         "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
                          "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * K, "clocks": clk,
         }
@@ -509,6 +541,14 @@ def run_reference(args, world):
     import oracle
 
     cores = len(os.sched_getaffinity(0))
+    full_B = w.B
+
+    def sample(n):  # the first n requests of the batch
+        out = dict(hc)
+        for k in ("target", "draft", "drafts", "temperature", "pos0", "block_table"):
+            out[k] = hc[k][:n]
+        out["hidden"] = hc["hidden"][:n * (w.K + 1)]
+        return out
 
     def step():
         if hc["kind"] == "probs":
@@ -523,13 +563,24 @@ def run_reference(args, world):
         oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], hc["hidden"],
                              hc["h_shared"])
 
+    # each step is a bounded sample of the batch (its first Bs requests), sized so that the
+    # warm-up and timed steps together take about two minutes at most
+    probe_n = min(full_B, 8)
+    full = hc
+    hc = sample(probe_n)
+    t0 = time.perf_counter()
+    step()
+    per_req = (time.perf_counter() - t0) / probe_n
+    Bs = int(max(1, min(full_B, 120.0 / max(1e-9, per_req * (args.steps + args.warmup)))))
+    hc = sample(Bs) if Bs != probe_n else hc
+    del full
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
-    value = w.B * args.steps / el
+    value = Bs * args.steps / el
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "requests/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -538,7 +589,8 @@ def run_reference(args, world):
         "data": "synthetic", "config": {"workload": workloads.config_label(cfg), "B": w.B,
                                         "K": w.K, "V": w.V, "H": w.H},
         "cpu_baseline": {"value": value, "unit": "requests/s", "cores": cores, "kind": "oracle",
-                         "sample": f"every step is the full batch of {w.B} requests"},
+                         "sample": f"every step verifies and rebuilds the first {Bs} of the "
+                                   f"batch's {full_B} requests"},
         "e2e": {"value": value, "unit": "requests/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
