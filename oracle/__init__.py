@@ -62,6 +62,13 @@ def _load():
         lib.oracle_accept_uniform.restype = ctypes.c_double
         lib.oracle_race_E.argtypes = [u64, u32, u32, u32]
         lib.oracle_race_E.restype = ctypes.c_float
+        lib.oracle_race_E_tag.argtypes = [u64, u32, u32, u32, u32]
+        lib.oracle_race_E_tag.restype = ctypes.c_float
+        sample_args = [i32, i32, i32, P, i64, P, u64, P, P, P, P, i32]
+        lib.oracle_draft_sample_probs.argtypes = sample_args
+        lib.oracle_draft_sample_probs.restype = i32
+        lib.oracle_draft_sample_logits.argtypes = sample_args
+        lib.oracle_draft_sample_logits.restype = i32
         lib.oracle_race_row_f32.argtypes = [P, P, i32, i32, u64, u32, u32, P]
         lib.oracle_race_row_f32.restype = i32
         verify_args = [i32, i32, i32, P, i64, P, i64, P, P, u64, P, P, P, P, P, P, P, P, i32]
@@ -99,8 +106,10 @@ def accept_uniform(seed: int, r: int, j: int) -> float:
     return _load().oracle_accept_uniform(seed, r, j)
 
 
-def race_E(seed: int, r: int, j: int, x: int) -> float:
-    return _load().oracle_race_E(seed, r, j, x)
+def race_E(seed: int, r: int, j: int, x: int, tag: int = 1) -> float:
+    if tag == 1:
+        return _load().oracle_race_E(seed, r, j, x)
+    return _load().oracle_race_E_tag(seed, r, j, x, tag)
 
 
 def race_row(p, q, seed, r, j):
@@ -169,6 +178,36 @@ def verify_logits(target_bits, draft_bits, drafts, temperature=None, seed=0, req
     B, K1, V = target_bits.shape
     return _verify(_load().oracle_verify_logits, B, K1 - 1, V, target_bits, V, draft_bits, V,
                    drafts, temperature, seed, req_ids, nthreads, margins)
+
+
+def _draft_sample(fn, rows, B, K, temperature, seed, req_ids, nthreads):
+    V = rows.shape[-1]
+    drafts = np.zeros((B, K), np.int32)
+    margin = np.zeros((B, K), np.float64)
+    err = np.zeros(1, np.int32)
+    temp = None if temperature is None else _c(temperature, np.float32)
+    rid = None if req_ids is None else _c(req_ids, np.int32)
+    rc = fn(B, K, V, _ptr(rows), V, _ptr(temp), seed, _ptr(rid), _ptr(drafts), _ptr(margin),
+            _ptr(err), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle draft sampling rejected its arguments (rc={rc})")
+    return dict(drafts=drafts, margin=margin, err=int(err[0]))
+
+
+def draft_sample_probs(q, temperature=None, seed=0, req_ids=None, nthreads=0):
+    """Drafter-side sampling on fp32 rows q [B, K, V] (reading R7)."""
+    q = _c(q, np.float32)
+    B, K, _ = q.shape
+    return _draft_sample(_load().oracle_draft_sample_probs, q, B, K, temperature, seed, req_ids,
+                         nthreads)
+
+
+def draft_sample_logits(logit_bits, temperature=None, seed=0, req_ids=None, nthreads=0):
+    """Drafter-side sampling on bf16 logit rows [B, K, V] given as uint16 bit patterns."""
+    lb = _c(logit_bits, np.uint16)
+    B, K, _ = lb.shape
+    return _draft_sample(_load().oracle_draft_sample_logits, lb, B, K, temperature, seed,
+                         req_ids, nthreads)
 
 
 def pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,

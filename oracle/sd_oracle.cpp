@@ -34,6 +34,10 @@
 //  R5 drafter slot j of request r takes target hidden row r*(K+1)+j for j <= a_r, MASK slots
 //     take h_shared (map -1); positions are pos0 + 1 + j.
 //  R6 is_rejected is over the verify batch [B, K+1]: 1 for draft slots j > a_r, 0 for slot 0.
+//  R7 drafter-side sampling (the drafter's K outputs per request become the next step's drafts):
+//     draft k of request r is the exponential race argmax_x q(x)/E_x over the drafter's row k,
+//     with E from word (x & 3) of block (x >> 2, k, r, 2) (tag 2, a stream of its own), the
+//     R2/R3 rules otherwise; temperature 0 takes argmax q, lowest index on ties.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fno-fast-math (no FMA contraction, so every
 // fp32 operation below is one IEEE-754 round-to-nearest operation on both x86-64 and aarch64).
@@ -95,9 +99,10 @@ double accept_uniform(uint64_t seed, uint32_t r, uint32_t j) {
   return (double)(w >> 8) * (1.0 / 16777216.0);
 }
 
-// R1/R2: the exponential variate E_x of vocab entry x on row j of request r.
-float race_E(uint64_t seed, uint32_t r, uint32_t j, uint32_t x) {
-  const uint32_t w = philox_word(seed, x >> 2, j, r, 1u, (int)(x & 3u));
+// R1/R2: the exponential variate E_x of vocab entry x on row j of request r (tag 1: the verify
+// races; tag 2: drafter-side sampling, R7).
+float race_E(uint64_t seed, uint32_t r, uint32_t j, uint32_t x, uint32_t tag = 1u) {
+  const uint32_t w = philox_word(seed, x >> 2, j, r, tag, (int)(x & 3u));
   const double v = ((double)w + 0.5) * (1.0 / 4294967296.0);
   return (float)(-std::log(v));
 }
@@ -198,6 +203,10 @@ double oracle_accept_uniform(uint64_t seed, uint32_t r, uint32_t j) {
 
 float oracle_race_E(uint64_t seed, uint32_t r, uint32_t j, uint32_t x) {
   return race_E(seed, r, j, x);
+}
+
+float oracle_race_E_tag(uint64_t seed, uint32_t r, uint32_t j, uint32_t x, uint32_t tag) {
+  return race_E(seed, r, j, x, tag);
 }
 
 // Exponential race on one row of fp32 values (exposed for the pin tests).
@@ -520,6 +529,112 @@ int oracle_hidden_gather(int capacity, int H, const int32_t* total_out, const in
     std::memcpy(out_hidden + i * ld_out, src, (size_t)H * sizeof(uint16_t));
   }
   if (err) *err |= e;
+  return 0;
+}
+
+// Drafter-side sampling (R7) on fp32 probability rows: row (i*K + k) at q + row*ld is the
+// drafter's distribution for draft k of request i. Keys q(x)/E_x are fp32 divisions (R3), the
+// largest wins, lowest x on ties; T == 0 takes the argmax. A row without a positive key gives
+// token 0 and ERR_ZERO_ROW. margin (nullable) [B*K] receives (k1 - k2) / k1.
+int oracle_draft_sample_probs(int B, int K, int V, const float* q, long ld,
+                              const float* temperature, uint64_t seed, const int32_t* req_ids,
+                              int32_t* drafts, double* margin, int32_t* err, int nthreads) {
+  if (B < 0 || K < 1 || V < 1) return -1;
+  std::vector<int32_t> errs((size_t)std::max(B, 1), 0);
+  parallel_for(B, nthreads, [&](int i) {
+    const uint32_t rid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
+    const bool greedy = temperature && temperature[i] == 0.0f;
+    for (int k = 0; k < K; ++k) {
+      const float* row = q + ((long)i * K + k) * ld;
+      double m = 0.0;
+      int x;
+      if (greedy) {
+        x = argmax_row([&](int t) { return (double)row[t]; }, V, &m);
+      } else {
+        int best_x = -1;
+        float best_k = 0.0f, second_k = 0.0f;
+        for (int t = 0; t < V; ++t) {
+          const float key = std::fmax(row[t], 0.0f) / race_E(seed, rid, (uint32_t)k, t, 2u);
+          if (key > best_k) {
+            second_k = best_k;
+            best_k = key;
+            best_x = t;
+          } else if (key > second_k) {
+            second_k = key;
+          }
+        }
+        m = best_k > 0.0f ? ((double)best_k - (double)second_k) / best_k : 0.0;
+        x = best_x;
+        if (x < 0) {
+          errs[i] |= ERR_ZERO_ROW;
+          x = 0;
+        }
+      }
+      drafts[(long)i * K + k] = x;
+      if (margin) margin[(long)i * K + k] = m;
+    }
+  });
+  if (err) {
+    int32_t e = 0;
+    for (int i = 0; i < B; ++i) e |= errs[i];
+    *err |= e;
+  }
+  return 0;
+}
+
+// Drafter-side sampling (R7) on bf16 logit rows: q = softmax(l / T) in double, keys q/E in
+// double; T == 0 takes the argmax of the raw logits.
+int oracle_draft_sample_logits(int B, int K, int V, const uint16_t* logits, long ld,
+                               const float* temperature, uint64_t seed, const int32_t* req_ids,
+                               int32_t* drafts, double* margin, int32_t* err, int nthreads) {
+  if (B < 0 || K < 1 || V < 1) return -1;
+  std::vector<int32_t> errs((size_t)std::max(B, 1), 0);
+  parallel_for(B, nthreads, [&](int i) {
+    const uint32_t rid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
+    const double T = temperature ? (double)temperature[i] : 1.0;
+    std::vector<double> qv((size_t)V);
+    for (int k = 0; k < K; ++k) {
+      const uint16_t* row = logits + ((long)i * K + k) * ld;
+      double m = 0.0;
+      int x;
+      if (T == 0.0) {
+        x = argmax_row([&](int t) { return (double)bf16_to_float(row[t]); }, V, &m);
+      } else {
+        double mx = -INFINITY;
+        for (int t = 0; t < V; ++t) mx = std::max(mx, (double)bf16_to_float(row[t]));
+        double S = 0.0;
+        for (int t = 0; t < V; ++t) {
+          qv[t] = std::exp(((double)bf16_to_float(row[t]) - mx) / T);
+          S += qv[t];
+        }
+        int best_x = -1;
+        double best_k = 0.0, second_k = 0.0;
+        for (int t = 0; t < V; ++t) {
+          const double key = (qv[t] / S) / (double)race_E(seed, rid, (uint32_t)k, t, 2u);
+          if (key > best_k) {
+            second_k = best_k;
+            best_k = key;
+            best_x = t;
+          } else if (key > second_k) {
+            second_k = key;
+          }
+        }
+        m = best_k > 0.0 ? (best_k - second_k) / best_k : 0.0;
+        x = best_x;
+        if (x < 0) {
+          errs[i] |= ERR_ZERO_ROW;
+          x = 0;
+        }
+      }
+      drafts[(long)i * K + k] = x;
+      if (margin) margin[(long)i * K + k] = m;
+    }
+  });
+  if (err) {
+    int32_t e = 0;
+    for (int i = 0; i < B; ++i) e |= errs[i];
+    *err |= e;
+  }
   return 0;
 }
 

@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   for (int q = tid; q < nreq; q += PNT) s_pos[q] = __ldg(P.pos0 + r0 + q);
   grid_dependency_wait();
 
+  // this CTA's first PNT accepted counts, loaded together with the prefix's (one round trip)
+  const int a_first = tid < nreq ? P.num_accepted[r0 + tid] : 0;
   // prefix over the requests before this CTA and the total over all requests
   long long pre = 0, tot = 0;
   for (int r = tid; r < P.B; r += PNT) {
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
     const int q = c + tid;
     int a = 0, L = 0;
     if (q < nreq) {
-      a = clamp_acc(P.num_accepted[r0 + q], K, e);
+      a = clamp_acc(c == 0 ? a_first : P.num_accepted[r0 + q], K, e);
       L = a + K;
     }
     int incl = L;
