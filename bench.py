@@ -165,6 +165,7 @@ def alloc_outputs(w, device):
     B, K, cap = w.B, w.K, w.capacity
     i32 = dict(dtype=torch.int32, device=device)
     return dict(out_tokens=torch.empty(B, K + 1, **i32), num_accepted=torch.empty(B, **i32),
+                next_drafts=torch.empty(B, K, **i32),
                 input_ids=torch.empty(cap, **i32), positions=torch.empty(cap, **i32),
                 slot_mapping=torch.empty(cap, **i32), hidden_map=torch.empty(cap, **i32),
                 is_masked=torch.empty(cap, dtype=torch.uint8, device=device),
@@ -208,6 +209,12 @@ def launch_verify(sd, w, o, stream=None):
     sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
                  temperature=temperatures(w), seed=w.seed, err=o["err"], stream=stream,
                  workspace_buf=o["ws"], request_base=getattr(w, "request_base", 0))
+
+
+def launch_draft_sample(sd, w, o, stream=None):
+    # the config's draft rows stand in for the drafter's outputs at new_token_idx
+    sd.sd_draft_sample(w.draft, o["next_drafts"], temperature=temperatures(w), seed=w.seed + 1,
+                       request_base=getattr(w, "request_base", 0), err=o["err"], stream=stream)
 
 
 def time_graph(fn, sets, outs, stream, K):
@@ -399,6 +406,9 @@ def main():
     # the dominant kernel alone, K launches in a graph of its own, right after the timed region
     avg_v = time_graph(lambda w, o, st: launch_verify(sd, w, o, st), sets, outs, stream, CHUNK)
     avg_p = time_graph(lambda w, o, st: launch_prepare(sd, w, o, st), sets, outs, stream, CHUNK)
+    # the next row of the method: drafter-side sampling of the K new drafts, timed alone
+    avg_s = time_graph(lambda w, o, st: launch_draft_sample(sd, w, o, st), sets, outs, stream,
+                       CHUNK)
     if world > 1:
         t = torch.tensor([total_ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -427,6 +437,14 @@ def main():
     launches = sd.sd_verify_kernels(B, sets[0].V, 0 if cfg["kind"] == "probs" else 1,
                                     temperatures(sets[0]) is not None) + 1
     a_all = np.concatenate([p[3] for p in per_set])
+    w0s = sets[0]
+    sample_bytes = w0s.B * w0s.K * w0s.V * w0s.draft.element_size() + w0s.B * w0s.K * 4 + w0s.B * 4
+    draft_sample = {"kernel": "sd_draft_sample", "us": avg_s * 1e3, "bytes_per_launch": sample_bytes,
+                    "achieved_GBps": sample_bytes / (avg_s * 1e-3) / 1e9,
+                    "frac": sample_bytes / (avg_s * 1e-3) / 1e9 / peak,
+                    "rows": f"B*K = {w0s.B * w0s.K} rows of V = {w0s.V}, each read once from HBM "
+                            "(logit rows: softmax statistics, then the race, the second pass "
+                            "mostly from L2)"}
     info = {
         "verify_ms": avg_v, "prepare_ms": avg_p,
         "step_ms_median": float(np.median(step_ms)) if step_ms else None,
@@ -464,6 +482,7 @@ def main():
                          "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
                          "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * K, "clocks": clk,
+            "draft_sample": draft_sample,
         }
         print(json.dumps(line))
     if world > 1:

@@ -159,6 +159,32 @@ SD_API int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target,
                              float* q_at_draft, int32_t* err, void* stream);
 
 /*
+ * sd_draft_sample -- the drafter's K new drafts per request, sampled from its output rows.
+ *
+ * P-EAGLE blog (vLLM), section "Triton Kernel": new_token_idx marks the drafter slots whose
+ * logits become the next drafts; the drafter runs its head on those slots, giving one row per
+ * (request, draft). Each row is sampled the way the verify step samples a bonus token
+ * (speculative-decoding explainer, "修正拒绝采样": an exact sample of the row's distribution):
+ * d_{k+1} of request r = argmax_x q(x) / E_x over row (r*K + k), E_x = fp32(-log((w + 0.5) 2^-32))
+ * with w word (x & 3) of Philox4x32-10 block (x >> 2, k, request_base + r, 2) -- tag 2, a stream
+ * separate from the verify races' tag 1 -- ties to the lowest x; temperature[r] == 0 takes the
+ * argmax of the row (lowest x on ties).
+ * Arguments:
+ *   rows: [B*K, V] with row stride ld elements: SD_F32_PROBS probabilities (already at the
+ *     sampling temperature; only temperature == 0 matters), or SD_BF16_LOGITS logits, sampled
+ *     from softmax(l / temperature[r]) computed in the kernel.
+ *   temperature: [B] fp32 or NULL (= 1); seed, request_base: as for sd_verify.
+ *   drafts: [B, K] int32 output (may serve as the next step's sd_verify drafts).
+ *   err: SD_ERR_ZERO_ROW when a sampled row has no positive entry (draft 0).
+ * Returns SD_OK, or SD_E_SHAPE (K outside [1, SD_K_MAX], V < 1, ld < V, B*K rows beyond 2^31
+ * CTAs, request_base + B > 2^32), SD_E_DTYPE, SD_E_NULL, SD_E_ALIGN (rows not aligned to its
+ * element), SD_E_DEVICE, SD_E_LAUNCH.
+ */
+SD_API int sd_draft_sample(int B, int K, int V, int dtype, const void* rows, long ld,
+                           const float* temperature, uint64_t seed, uint32_t request_base,
+                           int32_t* drafts, int32_t* err, void* stream);
+
+/*
  * sd_pdraft_expand -- rebuild of the drafter batch for P-EAGLE parallel drafting.
  *
  * P-EAGLE blog (vLLM), sections "核心方法" (drafter position i takes the token and hidden state

@@ -60,6 +60,14 @@ def test_host_argument_checks(lib):
     assert lib.sd_verify_kernels(0, 10, 0, 0) == 0
     # an empty batch is a no-op
     assert lib.sd_verify(0, 2, 10, 0, P, 10, P, 10, P, P, 0, 0, P, P, P, P, P, 0, P, P) == 0
+    # drafter-side sampling: K range, ld < V, dtype, request_base overflow, null rows, empty batch
+    assert lib.sd_draft_sample(2, 0, 10, 0, 16, 10, P, 0, 0, 16, P, P) == -2
+    assert lib.sd_draft_sample(2, 17, 10, 0, 16, 10, P, 0, 0, 16, P, P) == -2
+    assert lib.sd_draft_sample(2, 3, 10, 0, 16, 9, P, 0, 0, 16, P, P) == -2
+    assert lib.sd_draft_sample(2, 3, 10, 5, 16, 10, P, 0, 0, 16, P, P) == -3
+    assert lib.sd_draft_sample(2, 3, 10, 0, 16, 10, P, 0, 2**32 - 1, 16, P, P) == -2
+    assert lib.sd_draft_sample(2, 3, 10, 0, P, 10, P, 0, 0, 16, P, P) == -1
+    assert lib.sd_draft_sample(0, 3, 10, 0, P, 10, P, 0, 0, P, P, P) == 0
     # expand: block size 0, null outputs
     assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 0, 0, 4, *([P] * 11)) == -2
     assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 16, 0, 4, *([P] * 11)) == -1

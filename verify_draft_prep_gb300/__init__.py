@@ -30,7 +30,7 @@ SD_ERR_ZERO_ROW = 16
 SD_ERR_TOTAL_RANGE = 32
 
 EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
-            "sd_verify_noalloc", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+            "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -60,6 +60,8 @@ def load():
         lib.sd_verify_noalloc.restype = i32
         lib.sd_verify_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.sd_verify_workspace_bytes.restype = ctypes.c_size_t
+        lib.sd_draft_sample.argtypes = [i32, i32, i32, i32, P, i64, P, u64, u32, P, P, P]
+        lib.sd_draft_sample.restype = i32
         lib.sd_verify_kernels.argtypes = [i32, i32, i32, i32]
         lib.sd_verify_kernels.restype = i32
         lib.sd_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32, i32,
@@ -171,6 +173,30 @@ def sd_verify_kernels(B, V, dtype, has_temperature):
     if n < 0:
         raise SDError(f"sd_verify_kernels: {load().sd_status_string(n).decode()}")
     return n
+
+
+def sd_draft_sample(rows, drafts, temperature=None, seed=0, request_base=0, err=None,
+                    stream=None):
+    """Sample the drafter's K new drafts per request (see include/sd.h).
+
+    rows: [B*K, V] float32 probabilities or bfloat16 logits; drafts: [B, K] int32 (output);
+    temperature: [B] float32 or None; request_base: global request index of local request 0.
+    """
+    import torch
+
+    B, K = drafts.shape
+    V = rows.shape[1]
+    if rows.dtype == torch.float32:
+        dtype = SD_F32_PROBS
+    elif rows.dtype == torch.bfloat16:
+        dtype = SD_BF16_LOGITS
+    else:
+        raise SDError("rows must be float32 probabilities or bfloat16 logits")
+    if rows.shape[0] != B * K:
+        raise SDError("rows must hold B*K rows")
+    rc = load().sd_draft_sample(B, K, V, dtype, _ptr(rows), _row_stride(rows), _ptr(temperature),
+                                seed, request_base, _ptr(drafts), _ptr(err), _stream(rows, stream))
+    _check(rc, "sd_draft_sample")
 
 
 def sd_pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,

@@ -15,6 +15,8 @@ int sd_verify_noalloc_launch(int, int, int, int, const void*, long, const void*,
                              const int32_t*, const float*, uint64_t, uint32_t, int32_t*, int32_t*,
                              float*, float*, int32_t*, cudaStream_t);
 int sd_verify_kernel_count(int, int, int, int);
+int sd_sample_launch(int, int, int, int, const void*, long, const float*, uint64_t, uint32_t,
+                     int32_t*, int32_t*, cudaStream_t);
 int sd_prep_launch(int, int, const int32_t*, const int32_t*, const int32_t*, const int32_t*, int,
                    int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
                    int32_t*, int32_t*, int32_t*, int, const void*, long, int, const void*, void*,
@@ -102,6 +104,24 @@ int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, con
   return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
                           request_base, out_tokens, num_accepted, p_at_draft, q_at_draft,
                           workspace, err, (cudaStream_t)stream);
+}
+
+int sd_draft_sample(int B, int K, int V, int dtype, const void* rows, long ld,
+                    const float* temperature, uint64_t seed, uint32_t request_base,
+                    int32_t* drafts, int32_t* err, void* stream) {
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld < V) return SD_E_SHAPE;
+  // B*K rows of up to 8 CTAs each
+  if ((long long)B * K * 8 > 2147483647LL) return SD_E_SHAPE;
+  if ((unsigned long long)request_base + (unsigned long long)B > 4294967296ULL) return SD_E_SHAPE;
+  if (B == 0) return SD_OK;
+  if (!rows || !drafts) return SD_E_NULL;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  if ((uintptr_t)rows % esize) return SD_E_ALIGN;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_sample_launch(B, K, V, dtype, rows, ld, temperature, seed, request_base, drafts, err,
+                          (cudaStream_t)stream);
 }
 
 int sd_verify_noalloc(int B, int K, int V, int dtype, const void* target, long ld_t,

@@ -82,13 +82,16 @@ __device__ __forceinline__ double accept_uniform(PhiloxKey key, uint32_t r, uint
   return (double)(w.x >> 8) * (1.0 / 16777216.0);
 }
 
-// Race block of vocab entries 4g..4g+3 on row j of request r: block (g, j, r, 1).
-__device__ __forceinline__ uint4 race_block(PhiloxKey key, uint32_t g, uint32_t r, uint32_t j) {
-  return philox4x32_10(make_uint4(g, j, r, 1u), key);
+// Race block of vocab entries 4g..4g+3 on row j of request r: block (g, j, r, tag); tag 1 is
+// the verify races' stream, tag 2 the drafter-side sampling's.
+constexpr uint32_t kTagVerify = 1u, kTagDraft = 2u;
+__device__ __forceinline__ uint4 race_block(PhiloxKey key, uint32_t g, uint32_t r, uint32_t j,
+                                            uint32_t tag = kTagVerify) {
+  return philox4x32_10(make_uint4(g, j, r, tag), key);
 }
 __device__ __forceinline__ uint4 race_block(const PhiloxRoundKeys& rk, uint32_t g, uint32_t r,
-                                            uint32_t j) {
-  return philox4x32_10(make_uint4(g, j, r, 1u), rk);
+                                            uint32_t j, uint32_t tag = kTagVerify) {
+  return philox4x32_10(make_uint4(g, j, r, tag), rk);
 }
 __device__ __forceinline__ double accept_uniform(const PhiloxRoundKeys& rk, uint32_t r,
                                                  uint32_t j) {

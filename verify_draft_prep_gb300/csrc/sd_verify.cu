@@ -368,22 +368,23 @@ __device__ __forceinline__ float unit_max_alpha(const float (&r)[EPU], const uin
 
 template <class Src>
 __device__ __forceinline__ void unit_words(const PhiloxRoundKeys& rk, uint32_t u, uint32_t rid,
-                                           uint32_t j, uint4 (&w)[Src::EPU / 4]) {
+                                           uint32_t j, uint32_t tag, uint4 (&w)[Src::EPU / 4]) {
 #pragma unroll
-  for (int h = 0; h < Src::EPU / 4; ++h) w[h] = race_block(rk, u * (Src::EPU / 4) + h, rid, j);
+  for (int h = 0; h < Src::EPU / 4; ++h)
+    w[h] = race_block(rk, u * (Src::EPU / 4) + h, rid, j, tag);
 }
 
 // Exact keys of the positive elements of unit u, folded into `best` (one thread, rare path).
 template <class Src>
 __device__ __noinline__ void exact_unit(const Src& src, uint32_t u, const PhiloxRoundKeys& rk,
-                                        uint32_t rid, uint32_t j, uint64_t& best) {
+                                        uint32_t rid, uint32_t j, uint32_t tag, uint64_t& best) {
   constexpr int EPU = Src::EPU;
   typename Src::Raw raw;
   src.fetch(u, raw);
   float r[EPU];
   src.residual(raw, r);
   uint4 w[EPU / 4];
-  unit_words<Src>(rk, u, rid, j, w);
+  unit_words<Src>(rk, u, rid, j, tag, w);
 #pragma unroll
   for (int e = 0; e < EPU; ++e) {
     if (r[e] > 0.0f) {
@@ -420,7 +421,7 @@ __device__ __forceinline__ void race_take(const Src& src, const typename Src::Ra
 template <class Src>
 __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint32_t u1,
                                                const PhiloxRoundKeys& rk,
-                               uint32_t rid, uint32_t j, Smem& sm) {
+                               uint32_t rid, uint32_t j, Smem& sm, uint32_t tag = kTagVerify) {
   constexpr int EPU = Src::EPU, UNR = Src::UNR;
   float a1 = 0.0f, a2 = 0.0f;
   uint32_t best_u = 0xffffffffu;
@@ -437,7 +438,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
       for (int k = 0; k < UNR; ++k) {
         const uint32_t u = ub + k * NT;
         uint4 w[EPU / 4];
-        unit_words<Src>(rk, u, rid, j, w);
+        unit_words<Src>(rk, u, rid, j, tag, w);
         race_take(src, raw[k], w, u, a1, a2, best_u, &sm.tau);
         src.fetch_fast(u + UNR * NT, raw[k]);
       }
@@ -446,7 +447,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
     for (int k = 0; k < UNR; ++k) {  // drain the last UNR units in flight
       const uint32_t u = ub + k * NT;
       uint4 w[EPU / 4];
-      unit_words<Src>(rk, u, rid, j, w);
+      unit_words<Src>(rk, u, rid, j, tag, w);
       race_take(src, raw[k], w, u, a1, a2, best_u, &sm.tau);
     }
     ub += UNR * NT;
@@ -455,7 +456,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
     typename Src::Raw raw;
     src.fetch(ub, raw);
     uint4 w[EPU / 4];
-    unit_words<Src>(rk, ub, rid, j, w);
+    unit_words<Src>(rk, ub, rid, j, tag, w);
     race_take(src, raw, w, ub, a1, a2, best_u, &sm.tau);
   }
   if (threadIdx.x == 0) sm.ncand = 0;
@@ -481,10 +482,10 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
           float r[EPU];
           src.residual(raw, r);
           uint4 w[EPU / 4];
-          unit_words<Src>(rk, u, rid, j, w);
+          unit_words<Src>(rk, u, rid, j, tag, w);
           take = unit_max_alpha<EPU>(r, w, unit_wmax<EPU>(w)) * (1.0f + kBand) >= A;
         }
-        if (take) exact_unit(src, u, rk, rid, j, best);
+        if (take) exact_unit(src, u, rk, rid, j, tag, best);
       }
     }
     __syncthreads();
@@ -498,7 +499,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
           const uint32_t x = u * EPU + (uint32_t)(l % EPU);
           const float r = x < src.V ? src.at(x) : 0.0f;  // the last unit may pass the row end
           if (r > 0.0f) {
-            const uint4 w4 = race_block(rk, x >> 2, rid, j);
+            const uint4 w4 = race_block(rk, x >> 2, rid, j, tag);
             const uint64_t k = exact_key(r, word_of(w4, x & 3u), x);
             best = k > best ? k : best;
           }
@@ -914,7 +915,7 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
     for (int j = 0; j <= K; ++j) {
       const uint64_t pk =
           cluster_max_u64(argmax_chunk<DT>(trow(j), V, vec, u0, u1, sm), sm, phase, cl);
-      const uint32_t am = packed_index(pk);
+      const uint32_t am = pk ? packed_index(pk) : 0u;  // no value above -inf: entry 0
       if (j == K) {
         b = am;
         break;
@@ -1079,6 +1080,81 @@ __global__ void __launch_bounds__(NT, kRaceMinBlocks)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   race_role(P, blockIdx.x, sm, as);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- drafter-side sampling
+// Row (r*K + k) of `rows` is the drafter's output for draft k of request r: probabilities, or
+// logits turned into probabilities by the request's temperature. The new draft is the
+// exponential race argmax_x q(x)/E_x on the tag-2 Philox stream (block (x >> 2, k, r, 2)), or the
+// argmax at temperature 0 -- the verify kernel's bonus race and greedy scan on a row of their
+// own. One cluster of cl CTAs per row, each CTA a contiguous share of the row; logit rows take
+// the softmax statistics first (exchanged over the cluster), then the race.
+struct SampleParams {
+  int B, K, V;
+  const void* rows;
+  long ld;
+  const float* temperature;
+  PhiloxRoundKeys rk;
+  uint32_t rbase;
+  int32_t* drafts;
+  int32_t* err;
+  int cl;
+  int vec;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(NT, kMinBlocks) sample_kernel(const __grid_constant__ SampleParams P) {
+  __shared__ Smem sm;
+  constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int cl = P.cl;
+  const uint32_t crank = blockIdx.x % (unsigned)cl;
+  const int row = (int)(blockIdx.x / (unsigned)cl);
+  const int r = row / P.K, k = row - r * P.K;
+  const uint32_t V = (uint32_t)P.V;
+  const bool vec = P.vec != 0;
+  const uint32_t NU = (V + EPU - 1) / EPU;
+  const uint32_t u0 = (uint32_t)(((uint64_t)NU * crank) / (unsigned)cl);
+  const uint32_t u1 = (uint32_t)(((uint64_t)NU * (crank + 1)) / (unsigned)cl);
+  const float T = P.temperature ? P.temperature[r] : 1.0f;
+  const uint32_t rid = P.rbase + (uint32_t)r;
+  int phase = 0;
+  int32_t e = 0;
+  if (threadIdx.x == 0) sm.tau = 0u;
+  __syncthreads();
+  uint64_t pk;
+  if (T == 0.0f) {
+    const void* rp = DT == SD_F32_PROBS
+                         ? (const void*)((const float*)P.rows + (size_t)row * P.ld)
+                         : (const void*)((const uint16_t*)P.rows + (size_t)row * P.ld);
+    pk = cluster_max_u64(argmax_chunk<DT>(rp, V, vec, u0, u1, sm), sm, phase, cl);
+  } else if (DT == SD_F32_PROBS) {
+    F32Residual<false> src{(const float*)P.rows + (size_t)row * P.ld, nullptr, V, vec};
+    pk = cluster_max_u64(race_chunk(src, u0, u1, P.rk, rid, (uint32_t)k, sm, kTagDraft), sm,
+                         phase, cl);
+  } else {
+    const uint16_t* rp = (const uint16_t*)P.rows + (size_t)row * P.ld;
+    const float c = 1.4426950408889634f / T;
+    MaxSum st, unused;
+    row_stats<false>(rp, nullptr, V, vec, u0, u1, c, st, unused, sm, phase, cl);
+    Bf16Residual<false> src{rp, nullptr, st.m, 1.0f / st.s, 0.0f, 0.0f, c, V, vec};
+    pk = cluster_max_u64(race_chunk(src, u0, u1, P.rk, rid, (uint32_t)k, sm, kTagDraft), sm,
+                         phase, cl);
+  }
+  uint32_t b = 0;
+  if (T == 0.0f) {
+    b = pk ? packed_index(pk) : 0u;
+  } else if (packed_key_bits(pk) == 0u) {
+    e |= SD_ERR_ZERO_ROW;
+  } else {
+    b = packed_index(pk);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (crank == 0 && threadIdx.x == 0) {
+    P.drafts[row] = (int32_t)b;
+    raise_err(P.err, e);
+  }
+  if (cl > 1) cluster_barrier();  // peers may read this CTA's shared memory until here
 }
 
 }  // namespace sdk
@@ -1254,4 +1330,43 @@ extern "C" int sd_verify_noalloc_launch(int B, int K, int V, int dtype, const vo
   return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
                           request_base, out_tokens, num_accepted, p_at_draft, q_at_draft, slots,
                           err, stream);
+}
+
+// Drafter-side sampling: one cluster per row (the verify kernel's cluster size for V).
+extern "C" int sd_sample_launch(int B, int K, int V, int dtype, const void* rows, long ld,
+                                const float* temperature, uint64_t seed, uint32_t request_base,
+                                int32_t* drafts, int32_t* err, cudaStream_t stream) {
+  if (B == 0) return SD_OK;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  const int epu = dtype == SD_F32_PROBS ? 4 : 8;
+  sdk::SampleParams P;
+  P.B = B;
+  P.K = K;
+  P.V = V;
+  P.rows = rows;
+  P.ld = ld;
+  P.temperature = temperature;
+  P.rk = sdk::philox_round_keys(seed);
+  P.rbase = request_base;
+  P.drafts = drafts;
+  P.err = err;
+  P.cl = choose_cluster(V, epu);
+  P.vec = ((uintptr_t)rows % 16 == 0) && ((ld * esize) % 16 == 0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * K * P.cl), 1, 1);
+  cfg.blockDim = dim3(sdk::NT, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P.cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t rc;
+  if (dtype == SD_F32_PROBS) rc = cudaLaunchKernelEx(&cfg, sdk::sample_kernel<SD_F32_PROBS>, P);
+  else rc = cudaLaunchKernelEx(&cfg, sdk::sample_kernel<SD_BF16_LOGITS>, P);
+  return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
 }
