@@ -79,6 +79,10 @@ def _load():
         lib.oracle_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32,
                                              i32, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_pdraft_expand.restype = i32
+        lib.oracle_pdraft_prepare_padded.argtypes = [i32, i32, P, P, P, P, i32, i32,
+                                                     ctypes.c_int32, P, P, P, P, P, P, P, P,
+                                                     i32, P, i64, i32, P, P, i64, P]
+        lib.oracle_pdraft_prepare_padded.restype = i32
         lib.oracle_hidden_gather.argtypes = [i32, i32, P, P, P, i64, i32, P, P, i64, P]
         lib.oracle_hidden_gather.restype = i32
         _lib = lib
@@ -233,6 +237,38 @@ def pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_
         _ptr(o["start_loc"]), _ptr(o["new_token_idx"]), _ptr(o["total_out"]), _ptr(err))
     if rc != 0:
         raise ValueError(f"oracle expand rejected its arguments (rc={rc})")
+    o["err"] = int(err[0])
+    return o
+
+
+def pdraft_prepare_padded(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,
+                          target_hidden_bits, h_shared_bits):
+    """Padded drafter batch (reading R8): B rows of 2K slots, every output row written."""
+    out_tokens = _c(out_tokens, np.int32)
+    num_accepted = _c(num_accepted, np.int32)
+    pos0 = _c(pos0, np.int32)
+    block_table = _c(block_table, np.int32)
+    th = _c(target_hidden_bits, np.uint16)
+    hs = _c(h_shared_bits, np.uint16)
+    B, K1 = out_tokens.shape
+    K = K1 - 1
+    n = B * 2 * K
+    H = hs.shape[-1]
+    o = dict(input_ids=np.zeros(n, np.int32), positions=np.zeros(n, np.int32),
+             slot_mapping=np.zeros(n, np.int32), hidden_map=np.zeros(n, np.int32),
+             is_masked=np.zeros(n, np.uint8), rejected=np.zeros(n, np.uint8),
+             scatter_map=np.zeros(B * K1, np.int32), new_token_idx=np.zeros((B, K), np.int32),
+             out_hidden=np.zeros((n, H), np.uint16))
+    err = np.zeros(1, np.int32)
+    rc = _load().oracle_pdraft_prepare_padded(
+        B, K, _ptr(out_tokens), _ptr(num_accepted), _ptr(pos0), _ptr(block_table),
+        block_table.shape[1] if block_table.ndim == 2 else 0, block_size, mask_token_id,
+        _ptr(o["input_ids"]), _ptr(o["positions"]), _ptr(o["slot_mapping"]),
+        _ptr(o["hidden_map"]), _ptr(o["is_masked"]), _ptr(o["rejected"]), _ptr(o["scatter_map"]),
+        _ptr(o["new_token_idx"]), H, _ptr(th), H, th.shape[0], _ptr(hs), _ptr(o["out_hidden"]), H,
+        _ptr(err))
+    if rc != 0:
+        raise ValueError(f"oracle padded rebuild rejected its arguments (rc={rc})")
     o["err"] = int(err[0])
     return o
 

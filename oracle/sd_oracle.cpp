@@ -38,6 +38,13 @@
 //     draft k of request r is the exponential race argmax_x q(x)/E_x over the drafter's row k,
 //     with E from word (x & 3) of block (x >> 2, k, r, 2) (tag 2, a stream of its own), the
 //     R2/R3 rules otherwise; temperature 0 takes argmax q, lowest index on ties.
+//  R8 padded drafter batch ([PE] "Hidden State 管理": rejected tokens get PADDING_SLOT_ID; the
+//     target hidden states are scattered to their drafter rows): request r owns the fixed row of
+//     W = 2K slots [r*W, (r+1)*W). Slots j < a_r + K are those of the packed layout (R5);
+//     slots j >= a_r + K are rejected leftovers: token mask_token_id, position pos0 + 1 + j,
+//     KV slot -1, hidden map -1 (h_shared), is_masked 0, rejected 1. new_token_idx =
+//     r*W + a_r + k; the scatter map sends target row r*(K+1)+j to drafter row r*W + j for
+//     j <= a_r and is -1 for the rejected target rows.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fno-fast-math (no FMA contraction, so every
 // fp32 operation below is one IEEE-754 round-to-nearest operation on both x86-64 and aarch64).
@@ -500,6 +507,63 @@ int oracle_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t*
     slot_mapping[i] = -1;
     hidden_map[i] = -1;
     is_masked[i] = 0;
+  }
+  if (err) *err |= e;
+  return 0;
+}
+
+// Padded drafter batch (R8) with its hidden states: every one of the B*2K rows is written.
+int oracle_pdraft_prepare_padded(int B, int K, const int32_t* out_tokens,
+                                 const int32_t* num_accepted, const int32_t* pos0,
+                                 const int32_t* block_table, int max_blocks, int block_size,
+                                 int32_t mask_token_id, int32_t* input_ids, int32_t* positions,
+                                 int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked,
+                                 uint8_t* rejected, int32_t* scatter_map, int32_t* new_token_idx,
+                                 int H, const uint16_t* target_hidden, long ld_in, int n_in_rows,
+                                 const uint16_t* h_shared, uint16_t* out_hidden, long ld_out,
+                                 int32_t* err) {
+  if (B < 0 || K < 1 || block_size < 1 || max_blocks < 0 || H < 1) return -1;
+  const int W = 2 * K;
+  int32_t e = 0;
+  for (int r = 0; r < B; ++r) {
+    int a = num_accepted[r];
+    if (a < 0 || a > K) {
+      e |= ERR_NUM_ACCEPTED;
+      a = std::min(std::max(a, 0), K);
+    }
+    for (int j = 0; j < W; ++j) {
+      const long i = (long)r * W + j;
+      const bool live = j < a + K;
+      const long pos = (long)pos0[r] + 1 + j;
+      input_ids[i] = (j <= a) ? out_tokens[(long)r * (K + 1) + j] : mask_token_id;
+      positions[i] = (int32_t)pos;
+      int32_t slot = -1;
+      if (live) {
+        const long blk = pos >= 0 ? pos / block_size : -1;
+        if (blk < 0 || blk >= max_blocks) {
+          e |= ERR_BLOCK_TABLE;
+        } else {
+          const long phys = block_table[(long)r * max_blocks + blk];
+          const long sl = phys * block_size + pos % block_size;
+          if (phys < 0 || sl > 2147483647L) e |= ERR_BLOCK_TABLE;
+          else slot = (int32_t)sl;
+        }
+      }
+      slot_mapping[i] = slot;
+      long m = (j <= a) ? (long)r * (K + 1) + j : -1;
+      hidden_map[i] = (int32_t)m;
+      is_masked[i] = (live && j > a) ? 1 : 0;
+      rejected[i] = live ? 0 : 1;
+      if (m >= n_in_rows) {
+        e |= ERR_MAP_RANGE;
+        m = -1;
+      }
+      const uint16_t* src = m >= 0 ? target_hidden + m * ld_in : h_shared;
+      std::memcpy(out_hidden + i * ld_out, src, (size_t)H * sizeof(uint16_t));
+    }
+    for (int j = 0; j <= K; ++j)
+      scatter_map[(long)r * (K + 1) + j] = (j <= a) ? (int32_t)((long)r * W + j) : -1;
+    for (int k = 0; k < K; ++k) new_token_idx[(long)r * K + k] = (int32_t)((long)r * W + a + k);
   }
   if (err) *err |= e;
   return 0;
