@@ -239,6 +239,38 @@ SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int3
                              void* stream);
 
 /*
+ * sd_pdraft_prepare_padded -- the drafter batch in fixed-width rows, with its hidden states.
+ *
+ * P-EAGLE blog (vLLM), sections "并行草稿生成的挑战" and "Triton Kernel" (the rebuilt ids,
+ * positions, slot mapping, masks and new-token indices) and "Hidden State 管理" (rejected tokens
+ * map to PADDING_SLOT_ID = -1 so that they write no KV cache; the target hidden states are
+ * scattered to their drafter rows; MASK rows take h_shared). In this form every request keeps a
+ * row of W = 2K drafter slots whatever it accepted, so start indices are r*W, the batch size is
+ * fixed at B*W and no prefix over the batch is needed. Slot j of request r (i = r*W + j):
+ *   j < a_r + K: as sd_pdraft_expand defines slot j of request r (input_ids, positions =
+ *     pos0 + 1 + j, slot_mapping, hidden_map, is_masked), rejected[i] = 0;
+ *   j >= a_r + K (K - a_r rejected leftovers): input_ids = mask_token_id, positions =
+ *     pos0 + 1 + j, slot_mapping = -1, hidden_map = -1, is_masked = 0, rejected[i] = 1.
+ *   scatter_map [B*(K+1)]: target row r*(K+1)+j -> drafter row r*W + j for j <= a_r, else -1
+ *     (the same copies as hidden_map, indexed by source).
+ *   new_token_idx [B, K]: r*W + a_r + k.
+ *   out_hidden (nullable: metadata only) [B*W, H] bf16 with row stride ld_out: row i =
+ *     target_hidden[hidden_map[i]] or h_shared (also for map rows >= n_in_rows, with
+ *     SD_ERR_MAP_RANGE). Every row is written.
+ * Arguments as for sd_pdraft_prepare; outputs input_ids .. rejected have B*W entries.
+ * Errors: SD_ERR_NUM_ACCEPTED (clamped), SD_ERR_BLOCK_TABLE (live slot not covered: -1).
+ */
+SD_API int sd_pdraft_prepare_padded(int B, int K, const int32_t* out_tokens,
+                                    const int32_t* num_accepted, const int32_t* pos0,
+                                    const int32_t* block_table, int max_blocks, int block_size,
+                                    int32_t mask_token_id, int32_t* input_ids, int32_t* positions,
+                                    int32_t* slot_mapping, int32_t* hidden_map,
+                                    uint8_t* is_masked, uint8_t* rejected, int32_t* scatter_map,
+                                    int32_t* new_token_idx, int H, const void* target_hidden,
+                                    long ld_in, int n_in_rows, const void* h_shared,
+                                    void* out_hidden, long ld_out, int32_t* err, void* stream);
+
+/*
  * sd_hidden_gather -- drafter hidden states.
  *
  * P-EAGLE blog (vLLM), section "Hidden State 管理": target hidden states are copied to their

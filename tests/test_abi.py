@@ -68,6 +68,13 @@ def test_host_argument_checks(lib):
     assert lib.sd_draft_sample(2, 3, 10, 0, 16, 10, P, 0, 2**32 - 1, 16, P, P) == -2
     assert lib.sd_draft_sample(2, 3, 10, 0, P, 10, P, 0, 0, 16, P, P) == -1
     assert lib.sd_draft_sample(0, 3, 10, 0, P, 10, P, 0, 0, P, P, P) == 0
+    # padded rebuild: K range, null outputs, empty batch
+    assert lib.sd_pdraft_prepare_padded(1, 0, *([P] * 4), 1, 16, 0, *([P] * 8), 8, P, 8, 0, P, P,
+                                        8, P, P) == -2
+    assert lib.sd_pdraft_prepare_padded(1, 2, *([P] * 4), 1, 16, 0, *([P] * 8), 8, P, 8, 0, P, P,
+                                        8, P, P) == -1
+    assert lib.sd_pdraft_prepare_padded(0, 2, *([P] * 4), 1, 16, 0, *([P] * 8), 8, P, 8, 0, P, P,
+                                        8, P, P) == 0
     # expand: block size 0, null outputs
     assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 0, 0, 4, *([P] * 11)) == -2
     assert lib.sd_pdraft_expand(1, 2, P, P, P, P, 1, 16, 0, 4, *([P] * 11)) == -1

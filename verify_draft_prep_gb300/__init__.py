@@ -30,7 +30,7 @@ SD_ERR_ZERO_ROW = 16
 SD_ERR_TOTAL_RANGE = 32
 
 EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
-            "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+            "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_prepare_padded", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -71,6 +71,10 @@ def load():
                                           P, P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P, i64,
                                           P, P]
         lib.sd_pdraft_prepare.restype = i32
+        lib.sd_pdraft_prepare_padded.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32,
+                                                 P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P,
+                                                 i64, P, P]
+        lib.sd_pdraft_prepare_padded.restype = i32
         lib.sd_hidden_gather.argtypes = [i32, i32, P, P, P, i64, i32, P, P, i64, P, P]
         lib.sd_hidden_gather.restype = i32
         lib.sd_philox_words.argtypes = [i32, P, u64, P, P]
@@ -230,6 +234,29 @@ def sd_pdraft_prepare(out_tokens, num_accepted, pos0, block_table, block_size, m
         _row_stride(target_hidden), target_hidden.shape[0], _ptr(h_shared), _ptr(out_hidden),
         _row_stride(out_hidden), _ptr(err), _stream(start_loc, stream))
     _check(rc, "sd_pdraft_prepare")
+
+
+def sd_pdraft_prepare_padded(out_tokens, num_accepted, pos0, block_table, block_size,
+                             mask_token_id, input_ids, positions, slot_mapping, hidden_map,
+                             is_masked, rejected, scatter_map, new_token_idx, target_hidden=None,
+                             h_shared=None, out_hidden=None, err=None, stream=None):
+    """The drafter batch in fixed rows of 2K slots per request (see include/sd.h); outputs have
+    B*2K entries (out_hidden [B*2K, H] bf16, or None for the metadata alone)."""
+    B, K1 = out_tokens.shape
+    K = K1 - 1
+    if input_ids.shape[0] != B * 2 * K:
+        raise SDError("padded outputs have B*2K entries")
+    H = out_hidden.shape[1] if out_hidden is not None else 1
+    n_in = target_hidden.shape[0] if target_hidden is not None else 0
+    rc = load().sd_pdraft_prepare_padded(
+        B, K, _ptr(out_tokens), _ptr(num_accepted), _ptr(pos0), _ptr(block_table),
+        block_table.shape[1], block_size, mask_token_id, _ptr(input_ids), _ptr(positions),
+        _ptr(slot_mapping), _ptr(hidden_map), _ptr(is_masked), _ptr(rejected),
+        _ptr(scatter_map), _ptr(new_token_idx), H, _ptr(target_hidden),
+        _row_stride(target_hidden) if target_hidden is not None else H, n_in, _ptr(h_shared),
+        _ptr(out_hidden), _row_stride(out_hidden) if out_hidden is not None else H, _ptr(err),
+        _stream(input_ids, stream))
+    _check(rc, "sd_pdraft_prepare_padded")
 
 
 def sd_hidden_gather(total_out, hidden_map, target_hidden, h_shared, out_hidden, err=None,

@@ -21,6 +21,10 @@ int sd_prep_launch(int, int, const int32_t*, const int32_t*, const int32_t*, con
                    int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
                    int32_t*, int32_t*, int32_t*, int, const void*, long, int, const void*, void*,
                    long, int32_t*, cudaStream_t);
+int sd_prep_padded_launch(int, int, const int32_t*, const int32_t*, const int32_t*,
+                          const int32_t*, int, int, int32_t, int32_t*, int32_t*, int32_t*,
+                          int32_t*, uint8_t*, uint8_t*, int32_t*, int32_t*, int, const void*, long,
+                          int, const void*, void*, long, int32_t*, cudaStream_t);
 int sd_gather_launch(int, int, const int32_t*, const int32_t*, const void*, long, int,
                      const void*, void*, long, int32_t*, cudaStream_t);
 int sd_philox_launch(int, const uint32_t*, uint64_t, uint32_t*, cudaStream_t);
@@ -209,6 +213,37 @@ int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int32_t* nu
                         is_masked, is_rejected, start_loc, new_token_idx, total_out, H,
                         target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
                         (cudaStream_t)stream);
+}
+
+int sd_pdraft_prepare_padded(int B, int K, const int32_t* out_tokens,
+                             const int32_t* num_accepted, const int32_t* pos0,
+                             const int32_t* block_table, int max_blocks, int block_size,
+                             int32_t mask_token_id, int32_t* input_ids, int32_t* positions,
+                             int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked,
+                             uint8_t* rejected, int32_t* scatter_map, int32_t* new_token_idx,
+                             int H, const void* target_hidden, long ld_in, int n_in_rows,
+                             const void* h_shared, void* out_hidden, long ld_out, int32_t* err,
+                             void* stream) {
+  if (B < 0 || K < 1 || K > SD_K_MAX || max_blocks < 0 || block_size < 1) return SD_E_SHAPE;
+  if ((long long)B * 2 * K > 2147483647LL) return SD_E_SHAPE;
+  if (B == 0) return SD_OK;
+  if (!out_tokens || !num_accepted || !pos0 || (max_blocks > 0 && !block_table) || !input_ids ||
+      !positions || !slot_mapping || !hidden_map || !is_masked || !rejected || !scatter_map ||
+      !new_token_idx)
+    return SD_E_NULL;
+  if (out_hidden) {
+    if (H < 1 || ld_in < H || ld_out < H || n_in_rows < 0) return SD_E_SHAPE;
+    if (!h_shared || (n_in_rows > 0 && !target_hidden)) return SD_E_NULL;
+    if ((uintptr_t)target_hidden % 2 || (uintptr_t)h_shared % 2 || (uintptr_t)out_hidden % 2)
+      return SD_E_ALIGN;
+  }
+  const int rc = check_device();
+  if (rc != SD_OK) return rc;
+  return sd_prep_padded_launch(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks,
+                               block_size, mask_token_id, input_ids, positions, slot_mapping,
+                               hidden_map, is_masked, rejected, scatter_map, new_token_idx, H,
+                               target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
+                               (cudaStream_t)stream);
 }
 
 int sd_hidden_gather(int capacity, int H, const int32_t* total_out, const int32_t* hidden_map,

@@ -257,6 +257,113 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   if (tid == 0) raise_err(P.err, s_err);
 }
 
+// ------------------------------------------------------------------ padded drafter batch
+// The fixed-width form of the same rebuild (P-EAGLE blog, "Hidden State 管理": rejected tokens
+// are sent to PADDING_SLOT_ID = -1; target hidden states are scattered to their drafter rows):
+// request r owns drafter rows [r*2K, (r+1)*2K); its first a_r + K rows are the packed layout's,
+// the remaining K - a_r rows are rejected leftovers (token MASK, KV slot -1, hidden map -1 and
+// h_shared, rejected 1). No prefix is needed, so every row is independent: one warp per row, lane
+// 0 writing the row's metadata while the warp copies its hidden state.
+struct PaddedParams {
+  int B, K;
+  const int32_t* out_tokens;
+  const int32_t* num_accepted;
+  const int32_t* pos0;
+  const int32_t* block_table;
+  int max_blocks, block_size;
+  int32_t mask_id;
+  int32_t* input_ids;
+  int32_t* positions;
+  int32_t* slot_mapping;
+  int32_t* hidden_map;
+  uint8_t* is_masked;
+  uint8_t* rejected;
+  int32_t* scatter_map;
+  int32_t* new_token_idx;
+  int H;
+  const uint16_t* hidden;
+  long ld_in;
+  int n_in_rows;
+  const uint16_t* h_shared;
+  uint16_t* out_hidden;  // nullptr: metadata only
+  long ld_out;
+  int vec;
+  int32_t* err;
+};
+
+__global__ void __launch_bounds__(PNT) prep_padded_kernel(const PaddedParams P) {
+  __shared__ int s_err;
+  const int K = P.K, W = 2 * K;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (PNT / 32) + (threadIdx.x >> 5);
+  const long long n = (long long)P.B * W;
+  if (threadIdx.x == 0) s_err = 0;
+  const bool active = row < n;
+  const int r = active ? (int)(row / W) : 0, j = active ? (int)(row - (long long)r * W) : 0;
+  const int p0 = active ? __ldg(P.pos0 + r) : 0;  // not written by sd_verify
+  grid_dependency_wait();
+  __syncthreads();
+  int32_t e = 0;
+  if (active) {
+    const int a = clamp_acc(P.num_accepted[r], K, e);
+    const bool live = j < a + K;
+    long long m = (j <= a) ? (long long)r * (K + 1) + j : -1;
+    if (lane == 0) {
+      const long long pos = (long long)p0 + 1 + j;
+      int32_t slot = -1;
+      if (live) {
+        const long long blk = pos >= 0 ? pos / P.block_size : -1;
+        if (blk < 0 || blk >= P.max_blocks) {
+          e |= SD_ERR_BLOCK_TABLE;
+        } else {
+          const long long phys = __ldg(P.block_table + (size_t)r * P.max_blocks + blk);
+          const long long sl = phys * P.block_size + pos % P.block_size;
+          if (phys < 0 || sl > 2147483647LL) e |= SD_ERR_BLOCK_TABLE;
+          else slot = (int32_t)sl;
+        }
+      }
+      P.input_ids[row] = (j <= a) ? P.out_tokens[(size_t)r * (K + 1) + j] : P.mask_id;
+      P.positions[row] = (int32_t)pos;
+      P.slot_mapping[row] = slot;
+      P.hidden_map[row] = (int32_t)m;
+      P.is_masked[row] = (live && j > a) ? 1 : 0;
+      P.rejected[row] = live ? 0 : 1;
+      if (j <= K)
+        P.scatter_map[(size_t)r * (K + 1) + j] = (j <= a) ? (int32_t)((long long)r * W + j) : -1;
+      if (j < K) P.new_token_idx[(size_t)r * K + j] = (int32_t)((long long)r * W + a + j);
+    }
+    if (P.out_hidden) {
+      if (m >= P.n_in_rows) {
+        if (lane == 0) e |= SD_ERR_MAP_RANGE;
+        m = -1;
+      }
+      const uint16_t* src = m >= 0 ? P.hidden + m * P.ld_in : P.h_shared;
+      uint16_t* dst = P.out_hidden + row * P.ld_out;
+      if (P.vec) {
+        const int nv = P.H >> 3;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        int v = lane;
+        for (; v + 96 < nv; v += 128) {
+          const uint4 x0 = __ldg(s4 + v), x1 = __ldg(s4 + v + 32), x2 = __ldg(s4 + v + 64),
+                      x3 = __ldg(s4 + v + 96);
+          d4[v] = x0;
+          d4[v + 32] = x1;
+          d4[v + 64] = x2;
+          d4[v + 96] = x3;
+        }
+        for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
+      } else {
+        for (int x = lane; x < P.H; x += 32) dst[x] = __ldg(src + x);
+      }
+    }
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (e) atomicOr(&s_err, e);
+  __syncthreads();
+  if (threadIdx.x == 0) raise_err(P.err, s_err);
+}
+
 }  // namespace sdk
 
 extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
@@ -319,4 +426,59 @@ extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int
   if (out_hidden) rc = cudaLaunchKernelEx(&cfg, sdk::prep_kernel<true>, P);
   else rc = cudaLaunchKernelEx(&cfg, sdk::prep_kernel<false>, P);
   return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}
+
+extern "C" int sd_prep_padded_launch(int B, int K, const int32_t* out_tokens,
+                                     const int32_t* num_accepted, const int32_t* pos0,
+                                     const int32_t* block_table, int max_blocks, int block_size,
+                                     int32_t mask_token_id, int32_t* input_ids,
+                                     int32_t* positions, int32_t* slot_mapping,
+                                     int32_t* hidden_map, uint8_t* is_masked, uint8_t* rejected,
+                                     int32_t* scatter_map, int32_t* new_token_idx, int H,
+                                     const void* target_hidden, long ld_in, int n_in_rows,
+                                     const void* h_shared, void* out_hidden, long ld_out,
+                                     int32_t* err, cudaStream_t stream) {
+  if (B == 0) return SD_OK;
+  sdk::PaddedParams P;
+  P.B = B;
+  P.K = K;
+  P.out_tokens = out_tokens;
+  P.num_accepted = num_accepted;
+  P.pos0 = pos0;
+  P.block_table = block_table;
+  P.max_blocks = max_blocks;
+  P.block_size = block_size;
+  P.mask_id = mask_token_id;
+  P.input_ids = input_ids;
+  P.positions = positions;
+  P.slot_mapping = slot_mapping;
+  P.hidden_map = hidden_map;
+  P.is_masked = is_masked;
+  P.rejected = rejected;
+  P.scatter_map = scatter_map;
+  P.new_token_idx = new_token_idx;
+  P.H = H;
+  P.hidden = (const uint16_t*)target_hidden;
+  P.ld_in = ld_in;
+  P.n_in_rows = n_in_rows;
+  P.h_shared = (const uint16_t*)h_shared;
+  P.out_hidden = (uint16_t*)out_hidden;
+  P.ld_out = ld_out;
+  P.vec = out_hidden && (H % 8 == 0) && ((uintptr_t)target_hidden % 16 == 0) &&
+          ((uintptr_t)h_shared % 16 == 0) && ((uintptr_t)out_hidden % 16 == 0) &&
+          (ld_in % 8 == 0) && (ld_out % 8 == 0);
+  P.err = err;
+  const long long rows = (long long)B * 2 * K;
+  const long long grid = (rows + sdk::PNT / 32 - 1) / (sdk::PNT / 32);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(sdk::PNT, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sdk::prep_padded_kernel, P) == cudaSuccess ? SD_OK
+                                                                             : SD_E_LAUNCH;
 }
