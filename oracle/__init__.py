@@ -214,6 +214,47 @@ def draft_sample_logits(logit_bits, temperature=None, seed=0, req_ids=None, nthr
                          req_ids, nthreads)
 
 
+def verify_ragged(target, draft, drafts, cu, K_max, temperature=None, seed=0, logits=False,
+                  req_base=0, nthreads=0):
+    """Verify with a draft count per request: request r has K_r = cu[r+1] - cu[r] drafts, target
+    rows cu[r] + r .. cu[r] + r + K_r, draft rows and tokens cu[r] .. cu[r] + K_r - 1. Each
+    request is verified on its own, by the batch oracle with K = K_r and its own request index
+    (requests with equal K_r in one call). Outputs are padded to K_max like the library's."""
+    cu = np.asarray(cu, np.int64)
+    B = len(cu) - 1
+    ks = cu[1:] - cu[:-1]
+    out = dict(out_tokens=np.full((B, K_max + 1), -1, np.int32),
+               num_accepted=np.zeros(B, np.int32),
+               p_at_draft=np.full((B, K_max), -1.0, np.float32),
+               q_at_draft=np.full((B, K_max), -1.0, np.float32),
+               accept_margin=np.full((B, K_max), -1.0), race_margin=np.zeros(B), err=0)
+    temp = None if temperature is None else np.asarray(temperature, np.float32)
+    for k in sorted(set(ks.tolist())):
+        idx = np.nonzero(ks == k)[0]
+        t = np.stack([target[cu[r] + r: cu[r] + r + k + 1] for r in idx])
+        d = (np.stack([draft[cu[r]: cu[r] + k] for r in idx]) if k > 0
+             else np.zeros((len(idx), 0, target.shape[1]), target.dtype))
+        dr = (np.stack([drafts[cu[r]: cu[r] + k] for r in idx]) if k > 0
+              else np.zeros((len(idx), 0), np.int32))
+        T = None if temp is None else temp[idx]
+        rid = (idx + req_base).astype(np.int32)
+        if logits:
+            res = verify_logits(t, d, dr, temperature=T, seed=seed, req_ids=rid,
+                                nthreads=nthreads, margins=True)
+        else:
+            res = verify_probs(t, d, dr, temperature=T, seed=seed, req_ids=rid,
+                               nthreads=nthreads)
+        out["out_tokens"][idx, :k + 1] = res["out_tokens"]
+        out["num_accepted"][idx] = res["num_accepted"]
+        out["p_at_draft"][idx, :k] = res["p_at_draft"]
+        out["q_at_draft"][idx, :k] = res["q_at_draft"]
+        if logits:
+            out["accept_margin"][idx, :k] = res["accept_margin"]
+            out["race_margin"][idx] = res["race_margin"]
+        out["err"] |= res["err"]
+    return out
+
+
 def pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,
                   capacity=None):
     out_tokens = _c(out_tokens, np.int32)

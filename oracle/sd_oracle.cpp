@@ -234,7 +234,7 @@ int oracle_verify_probs(int B, int K, int V, const float* target, long ld_t, con
                         const int32_t* req_ids, int32_t* out_tokens, int32_t* num_accepted,
                         float* p_at, float* q_at, double* acc_margin, double* race_margin,
                         int32_t* err, int nthreads) {
-  if (B < 0 || K < 1 || V < 1) return -1;
+  if (B < 0 || K < 0 || V < 1) return -1;  // K == 0: the bonus token from p_0 alone
   std::vector<int32_t> errs((size_t)std::max(B, 1), 0);
   parallel_for(B, nthreads, [&](int i) {
     const uint32_t rid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
@@ -328,7 +328,7 @@ int oracle_verify_logits(int B, int K, int V, const uint16_t* target, long ld_t,
                          const float* temperature, uint64_t seed, const int32_t* req_ids,
                          int32_t* out_tokens, int32_t* num_accepted, float* p_at, float* q_at,
                          double* acc_margin, double* race_margin, int32_t* err, int nthreads) {
-  if (B < 0 || K < 1 || V < 1) return -1;
+  if (B < 0 || K < 0 || V < 1) return -1;  // K == 0: the bonus token from p_0 alone
   std::vector<int32_t> errs((size_t)std::max(B, 1), 0);
   parallel_for(B, nthreads, [&](int i) {
     const uint32_t rid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
