@@ -166,6 +166,12 @@ def alloc_outputs(w, device):
     i32 = dict(dtype=torch.int32, device=device)
     return dict(out_tokens=torch.empty(B, K + 1, **i32), num_accepted=torch.empty(B, **i32),
                 next_drafts=torch.empty(B, K, **i32),
+                pad_ids=torch.empty(B * 2 * K, **i32), pad_pos=torch.empty(B * 2 * K, **i32),
+                pad_slot=torch.empty(B * 2 * K, **i32), pad_map=torch.empty(B * 2 * K, **i32),
+                pad_masked=torch.empty(B * 2 * K, dtype=torch.uint8, device=device),
+                pad_rej=torch.empty(B * 2 * K, dtype=torch.uint8, device=device),
+                pad_scatter=torch.empty(B * (K + 1), **i32), pad_nti=torch.empty(B, K, **i32),
+                pad_hidden=torch.empty(B * 2 * K, w.H, dtype=torch.bfloat16, device=device),
                 input_ids=torch.empty(cap, **i32), positions=torch.empty(cap, **i32),
                 slot_mapping=torch.empty(cap, **i32), hidden_map=torch.empty(cap, **i32),
                 is_masked=torch.empty(cap, dtype=torch.uint8, device=device),
@@ -215,6 +221,15 @@ def launch_draft_sample(sd, w, o, stream=None):
     # the config's draft rows stand in for the drafter's outputs at new_token_idx
     sd.sd_draft_sample(w.draft, o["next_drafts"], temperature=temperatures(w), seed=w.seed + 1,
                        request_base=getattr(w, "request_base", 0), err=o["err"], stream=stream)
+
+
+def launch_prepare_padded(sd, w, o, stream=None):
+    sd.sd_pdraft_prepare_padded(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table,
+                                w.block_size, w.mask_token_id, o["pad_ids"], o["pad_pos"],
+                                o["pad_slot"], o["pad_map"], o["pad_masked"], o["pad_rej"],
+                                o["pad_scatter"], o["pad_nti"], target_hidden=w.hidden,
+                                h_shared=w.h_shared, out_hidden=o["pad_hidden"], err=o["err"],
+                                stream=stream)
 
 
 def time_graph(fn, sets, outs, stream, K):
@@ -406,6 +421,9 @@ def main():
     # the dominant kernel alone, K launches in a graph of its own, right after the timed region
     avg_v = time_graph(lambda w, o, st: launch_verify(sd, w, o, st), sets, outs, stream, CHUNK)
     avg_p = time_graph(lambda w, o, st: launch_prepare(sd, w, o, st), sets, outs, stream, CHUNK)
+    # the padded form of the rebuild (fixed 2K-slot rows), timed alone after the same verify
+    avg_pp = time_graph(lambda w, o, st: launch_prepare_padded(sd, w, o, st), sets, outs, stream,
+                        CHUNK)
     # the next row of the method: drafter-side sampling of the K new drafts, timed alone
     avg_s = time_graph(lambda w, o, st: launch_draft_sample(sd, w, o, st), sets, outs, stream,
                        CHUNK)
@@ -439,6 +457,15 @@ def main():
     a_all = np.concatenate([p[3] for p in per_set])
     w0s = sets[0]
     sample_bytes = w0s.B * w0s.K * w0s.V * w0s.draft.element_size() + w0s.B * w0s.K * 4 + w0s.B * 4
+    pad_bytes = float(np.mean([
+        int(((per_set[s % nsets][3] + 1) * 2 * w0s.H).sum()) + w0s.B * 2 * w0s.K * (2 * w0s.H + 18)
+        + w0s.B * (w0s.K + 1) * 4 + w0s.B * w0s.K * 4 for s in range(CHUNK)]))
+    prepare_padded = {"kernel": "sd_pdraft_prepare_padded", "us": avg_pp * 1e3,
+                      "bytes_per_launch": pad_bytes,
+                      "achieved_GBps": pad_bytes / (avg_pp * 1e-3) / 1e9,
+                      "frac": pad_bytes / (avg_pp * 1e-3) / 1e9 / peak,
+                      "rows": f"B*2K = {w0s.B * 2 * w0s.K} drafter rows, every one written "
+                              "(hidden states read for the a_r + 1 target rows of each request)"}
     draft_sample = {"kernel": "sd_draft_sample", "us": avg_s * 1e3, "bytes_per_launch": sample_bytes,
                     "achieved_GBps": sample_bytes / (avg_s * 1e-3) / 1e9,
                     "frac": sample_bytes / (avg_s * 1e-3) / 1e9 / peak,
@@ -482,7 +509,7 @@ def main():
                          "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
                          "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * K, "clocks": clk,
-            "draft_sample": draft_sample,
+            "draft_sample": draft_sample, "prepare_padded": prepare_padded,
         }
         print(json.dumps(line))
     if world > 1:

@@ -59,6 +59,8 @@ extern "C" {
 #define SD_ERR_MAP_RANGE 8      /* hidden_map row >= n_in_rows: h_shared written instead */
 #define SD_ERR_ZERO_ROW 16      /* a race row without a positive key even on p: token 0 */
 #define SD_ERR_TOTAL_RANGE 32   /* total_out outside [0, capacity]: clamped */
+#define SD_ERR_DRAFT_COUNT 128  /* cu_drafts gives a request a draft count outside [0, K_max]:
+                                   clamped (sd_verify_ragged) */
 
 /* input kinds for sd_verify */
 #define SD_F32_PROBS 0    /* fp32 probabilities, already at the sampling temperature */
@@ -117,6 +119,28 @@ SD_API int sd_verify(int B, int K, int V, int dtype, const void* target, long ld
                      int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft,
                      float* q_at_draft, void* workspace, size_t workspace_bytes, int32_t* err,
                      void* stream);
+
+/*
+ * sd_verify_ragged -- sd_verify with a number of drafts of its own for every request.
+ *
+ * Request r has K_r = cu_drafts[r+1] - cu_drafts[r] drafts (0 <= K_r <= K_max; cu_drafts is the
+ * exclusive prefix [B+1] of the counts, on the device). Its rows are packed: target rows
+ * p_0..p_{K_r} at rows cu_drafts[r] + r .. cu_drafts[r] + r + K_r of target, draft rows
+ * q_0..q_{K_r - 1} and draft tokens at cu_drafts[r] .. of draft and drafts. Each request is
+ * verified exactly as sd_verify verifies it with K = K_r (the same Philox counters: request
+ * request_base + r, row j); K_r = 0 samples the bonus token from p_0 alone. Outputs keep the
+ * stride of K_max: out_tokens [B, K_max+1] (-1 after b_r), p_at_draft / q_at_draft [B, K_max]
+ * (-1 where no draft was examined). cu_drafts must be consistent with the arrays: rows are
+ * addressed from its entries. A count outside [0, K_max] (a decreasing entry, a step beyond K_max)
+ * is clamped and raises SD_ERR_DRAFT_COUNT; the rows it then addresses must still lie inside the
+ * arrays. Other arguments, workspace and errors as for sd_verify (with K = K_max).
+ */
+SD_API int sd_verify_ragged(int B, int K_max, int V, int dtype, const void* target, long ld_t,
+                            const void* draft, long ld_d, const int32_t* drafts,
+                            const int32_t* cu_drafts, const float* temperature, uint64_t seed,
+                            uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
+                            float* p_at_draft, float* q_at_draft, void* workspace,
+                            size_t workspace_bytes, int32_t* err, void* stream);
 
 /*
  * Size in bytes of the workspace sd_verify needs for B requests: 16 bytes per request, where the

@@ -28,9 +28,11 @@ SD_ERR_NUM_ACCEPTED = 4
 SD_ERR_MAP_RANGE = 8
 SD_ERR_ZERO_ROW = 16
 SD_ERR_TOTAL_RANGE = 32
+SD_ERR_DRAFT_COUNT = 128
 
 EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
-            "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_prepare_padded", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+            "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_prepare_padded",
+            "sd_verify_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -55,6 +57,9 @@ def load():
         lib.sd_verify.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, u32, P, P, P,
                                   P, P, ctypes.c_size_t, P, P]
         lib.sd_verify.restype = i32
+        lib.sd_verify_ragged.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, P, u64, u32, P,
+                                         P, P, P, P, ctypes.c_size_t, P, P]
+        lib.sd_verify_ragged.restype = i32
         lib.sd_verify_noalloc.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64, u32, P,
                                           P, P, P, P, P]
         lib.sd_verify_noalloc.restype = i32
@@ -169,6 +174,37 @@ def sd_verify(target, draft, drafts, out_tokens, num_accepted, temperature=None,
                           _ptr(q_at_draft), _ptr(ws), ws.numel(), _ptr(err),
                           _stream(target, stream))
     _check(rc, "sd_verify")
+
+
+def sd_verify_ragged(target, draft, drafts, cu_drafts, out_tokens, num_accepted, temperature=None,
+                     seed=0, p_at_draft=None, q_at_draft=None, err=None, stream=None,
+                     workspace_buf=None, request_base=0):
+    """Verify with a draft count per request (see include/sd.h).
+
+    cu_drafts: [B+1] int32 exclusive prefix of the counts; target: [cu[B] + B, V] rows;
+    draft: [cu[B], V]; drafts: [cu[B]] int32; out_tokens: [B, K_max+1]; p/q_at: [B, K_max].
+    """
+    import torch
+
+    B, K1 = out_tokens.shape
+    V = target.shape[1]
+    if target.dtype == torch.float32:
+        dtype = SD_F32_PROBS
+    elif target.dtype == torch.bfloat16:
+        dtype = SD_BF16_LOGITS
+    else:
+        raise SDError("target must be float32 probabilities or bfloat16 logits")
+    if draft.dtype != target.dtype or cu_drafts.shape[0] != B + 1:
+        raise SDError("draft must match target; cu_drafts needs B+1 entries")
+    ws = workspace_buf if workspace_buf is not None else workspace(target.device, B, K1 - 1, V,
+                                                                   dtype)
+    rc = load().sd_verify_ragged(B, K1 - 1, V, dtype, _ptr(target), _row_stride(target),
+                                 _ptr(draft), _row_stride(draft) if draft.shape[0] else V,
+                                 _ptr(drafts), _ptr(cu_drafts), _ptr(temperature), seed,
+                                 request_base, _ptr(out_tokens), _ptr(num_accepted),
+                                 _ptr(p_at_draft), _ptr(q_at_draft), _ptr(ws), ws.numel(),
+                                 _ptr(err), _stream(target, stream))
+    _check(rc, "sd_verify_ragged")
 
 
 def sd_verify_kernels(B, V, dtype, has_temperature):

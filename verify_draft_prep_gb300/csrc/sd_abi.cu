@@ -8,8 +8,8 @@
 
 extern "C" {
 int sd_verify_launch(int, int, int, int, const void*, long, const void*, long, const int32_t*,
-                     const float*, uint64_t, uint32_t, int32_t*, int32_t*, float*, float*, void*,
-                     int32_t*, cudaStream_t);
+                     const int32_t*, const float*, uint64_t, uint32_t, int32_t*, int32_t*, float*,
+                     float*, void*, int32_t*, cudaStream_t);
 size_t sd_verify_workspace_launch(int);
 int sd_verify_noalloc_launch(int, int, int, int, const void*, long, const void*, long,
                              const int32_t*, const float*, uint64_t, uint32_t, int32_t*, int32_t*,
@@ -105,9 +105,34 @@ int sd_verify(int B, int K, int V, int dtype, const void* target, long ld_t, con
   if ((uintptr_t)workspace % 16) return SD_E_ALIGN;
   const int dev = check_device();
   if (dev != SD_OK) return dev;
-  return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
-                          request_base, out_tokens, num_accepted, p_at_draft, q_at_draft,
-                          workspace, err, (cudaStream_t)stream);
+  return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, nullptr,
+                          temperature, seed, request_base, out_tokens, num_accepted, p_at_draft,
+                          q_at_draft, workspace, err, (cudaStream_t)stream);
+}
+
+int sd_verify_ragged(int B, int K_max, int V, int dtype, const void* target, long ld_t,
+                     const void* draft, long ld_d, const int32_t* drafts,
+                     const int32_t* cu_drafts, const float* temperature, uint64_t seed,
+                     uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
+                     float* p_at_draft, float* q_at_draft, void* workspace,
+                     size_t workspace_bytes, int32_t* err, void* stream) {
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K_max < 1 || K_max > SD_K_MAX || V < 1 || ld_t < V || ld_d < V)
+    return SD_E_SHAPE;
+  if ((long long)B * (K_max + 1) > 2147483647LL) return SD_E_SHAPE;
+  if ((unsigned long long)request_base + (unsigned long long)B > 4294967296ULL) return SD_E_SHAPE;
+  if (B == 0) return SD_OK;
+  if (!target || !draft || !drafts || !cu_drafts || !out_tokens || !num_accepted || !workspace)
+    return SD_E_NULL;
+  if (workspace_bytes < sd_verify_workspace_bytes(B, K_max, V, dtype)) return SD_E_SHAPE;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  if ((uintptr_t)target % esize || (uintptr_t)draft % esize) return SD_E_ALIGN;
+  if ((uintptr_t)workspace % 16) return SD_E_ALIGN;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_verify_launch(B, K_max, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts,
+                          temperature, seed, request_base, out_tokens, num_accepted, p_at_draft,
+                          q_at_draft, workspace, err, (cudaStream_t)stream);
 }
 
 int sd_draft_sample(int B, int K, int V, int dtype, const void* rows, long ld,

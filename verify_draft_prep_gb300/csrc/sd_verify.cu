@@ -64,6 +64,7 @@ struct VerifyParams {
   long ld_d;
   const int32_t* drafts;
   const float* temperature;
+  const int32_t* cu;  // nullable: per-request draft counts as a prefix [B+1] (K is then K_max)
   PhiloxRoundKeys rk;
   uint32_t rbase;  // request index of row 0 in the Philox counters (global index of a shard)
   int32_t* out_tokens;
@@ -79,6 +80,27 @@ struct VerifyParams {
                        // request in the cluster role)
   int vec;  // 1: every row starts on a 16-byte boundary
 };
+
+// Request r's rows: K_r drafts (cu[r+1] - cu[r] when per-request counts are given, clamped to
+// [0, K] with SD_ERR_DRAFT_COUNT; else K), target rows t0 .. t0 + K_r (t0 = cu[r] + r, or
+// r*(K+1)), draft rows and draft tokens from d0 (cu[r], or r*K). Outputs keep the stride of K.
+struct ReqRows {
+  int k;
+  size_t t0, d0;
+  int32_t e;
+};
+__device__ __forceinline__ ReqRows req_rows(const VerifyParams& P, int r) {
+  if (!P.cu) return ReqRows{P.K, (size_t)r * (P.K + 1), (size_t)r * P.K, 0};
+  const int c0 = __ldg(P.cu + r), c1 = __ldg(P.cu + r + 1);
+  int k = c1 - c0;
+  int32_t e = 0;
+  if (k < 0 || k > P.K || c0 < 0) {
+    e = SD_ERR_DRAFT_COUNT;
+    k = c0 < 0 ? 0 : (k < 0 ? 0 : P.K);
+  }
+  const size_t base = c0 < 0 ? 0 : (size_t)c0;
+  return ReqRows{k, base + (size_t)r, base, e};
+}
 
 // ---------------------------------------------------------------------------------- row sources
 // A "unit" is 16 bytes of a row: 4 fp32 or 8 bf16 elements. Units past V (the ragged tail) and
@@ -709,15 +731,16 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
 // go to Ps/Qs (others stay as they are). Returns a_r; *bad_out receives SD_ERR_TOKEN_RANGE when
 // the first rejection came from an out-of-range draft.
 __device__ int accept_scan_warp(const VerifyParams& P, int r, float* Ps, float* Qs, int* bad_out) {
-  const int K = P.K;
+  const ReqRows rr = req_rows(P, r);
+  const int K = rr.k;
   const uint32_t V = (uint32_t)P.V;
   const int j = threadIdx.x & 31;
-  const float* trow = (const float*)P.target + ((size_t)r * (K + 1) + j) * P.ld_t;
-  const float* drow = (const float*)P.draft + ((size_t)r * K + j) * P.ld_d;
+  const float* trow = (const float*)P.target + (rr.t0 + j) * P.ld_t;
+  const float* drow = (const float*)P.draft + (rr.d0 + j) * P.ld_d;
   bool acc = false, bad = false;
   float Pv = 0.0f, Qv = 0.0f;
   if (j < K) {
-    const int d = __ldg(P.drafts + (size_t)r * K + j);
+    const int d = __ldg(P.drafts + rr.d0 + j);
     if (d >= 0 && (uint32_t)d < V) {
       Pv = __ldg(trow + d);
       Qv = __ldg(drow + d);
@@ -734,7 +757,7 @@ __device__ int accept_scan_warp(const VerifyParams& P, int r, float* Ps, float* 
     Qs[j] = Qv;
   }
   const unsigned badm = __ballot_sync(0xffffffffu, bad && j == av);
-  *bad_out = badm ? SD_ERR_TOKEN_RANGE : 0;
+  *bad_out = (badm ? SD_ERR_TOKEN_RANGE : 0) | rr.e;
   return av;
 }
 
@@ -742,10 +765,11 @@ __device__ int accept_scan_warp(const VerifyParams& P, int r, float* Ps, float* 
 __device__ void write_request(const VerifyParams& P, int r, int a, uint32_t b, int32_t e,
                               const float* Ps, const float* Qs) {
   const int K = P.K;
+  const size_t d0 = req_rows(P, r).d0;
   const int t = threadIdx.x;
   if (t <= K) {
     int32_t tok = -1;
-    if (t < a) tok = __ldg(P.drafts + (size_t)r * K + t);
+    if (t < a) tok = __ldg(P.drafts + d0 + t);
     else if (t == a) tok = (int32_t)b;
     P.out_tokens[(size_t)r * (K + 1) + t] = tok;
   }
@@ -785,12 +809,13 @@ __device__ bool merge_slot(RaceSlot* slot, uint64_t pk, uint32_t units, uint32_t
 __device__ __noinline__ void finish_sampled(const VerifyParams& P, int r, int a, int32_t e,
                                             uint64_t pk,
                                const float* Ps, const float* Qs, Smem& sm) {
-  const int K = P.K;
+  const ReqRows rr = req_rows(P, r);
+  const int K = rr.k;
   const uint32_t V = (uint32_t)P.V;
   const uint32_t NU = (V + 3u) / 4u;
   const bool vec = P.vec != 0;
   const int jr = a < K ? a : K;
-  const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
+  const float* prow = (const float*)P.target + (rr.t0 + jr) * P.ld_t;
   if (packed_key_bits(pk) == 0u && a < K) {
     // no positive residual key anywhere in the row: race on p of the same row, whole row
     F32Residual<false> src{prow, nullptr, V, vec};
@@ -821,7 +846,6 @@ struct AcceptState {
 
 __device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Smem& sm,
                                           AcceptState& as) {
-  const int K = P.K;
   const uint32_t V = (uint32_t)P.V;
   const uint32_t NU = (V + 3u) / 4u;
   const bool vec = P.vec != 0;
@@ -852,9 +876,11 @@ __device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Sme
     const uint32_t hi = (uint32_t)(min(w1, base + NU) - base);
     const int i = r - r0;
     const int a = as.a[i];
+    const ReqRows rr = req_rows(P, r);
+    const int K = rr.k;
     const int jr = a < K ? a : K;
-    const float* prow = (const float*)P.target + ((size_t)r * (K + 1) + jr) * P.ld_t;
-    const float* qrow = a < K ? (const float*)P.draft + ((size_t)r * K + jr) * P.ld_d : nullptr;
+    const float* prow = (const float*)P.target + (rr.t0 + jr) * P.ld_t;
+    const float* qrow = a < K ? (const float*)P.draft + (rr.d0 + jr) * P.ld_d : nullptr;
     const F32ResidualAny src{prow, qrow, V, vec};
     const uint64_t pk = race_chunk(src, lo, hi, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     uint64_t row_max;
@@ -875,15 +901,17 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
   const int nc = P.nc;
   const uint32_t rank = blockIdx.x % (unsigned)nc;  // this CTA's index within its request
   const int r = (int)(blockIdx.x / (unsigned)nc);
-  const int K = P.K;
+  const ReqRows rr = req_rows(P, r);
+  const int K = rr.k;    // this request's drafts
+  const int KM = P.K;    // the output stride
   const uint32_t V = (uint32_t)P.V;
   const bool vec = P.vec != 0;
   const uint32_t NU = (V + EPU - 1) / EPU;
-  const Elt* tbase = (const Elt*)P.target + (size_t)r * (K + 1) * P.ld_t;
-  const Elt* dbase = (const Elt*)P.draft + (size_t)r * K * P.ld_d;
+  const Elt* tbase = (const Elt*)P.target + rr.t0 * P.ld_t;
+  const Elt* dbase = (const Elt*)P.draft + rr.d0 * P.ld_d;
   auto trow = [&](int j) { return tbase + (size_t)j * P.ld_t; };
   auto drow = [&](int j) { return dbase + (size_t)j * P.ld_d; };
-  const int32_t* dr = P.drafts + (size_t)r * K;
+  const int32_t* dr = P.drafts + rr.d0;
   const float T = P.temperature ? P.temperature[r] : 1.0f;
   const bool greedy = (T == 0.0f);
   const bool sampled_probs = DT == SD_F32_PROBS && !greedy;
@@ -899,7 +927,7 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
   int phase = 0;
   int a = K;
   uint32_t b = 0;
-  int32_t e = 0;
+  int32_t e = rr.e;
   bool writer = crank == 0;  // the CTA that writes the request's outputs
   const int lane = threadIdx.x & 31;
 
@@ -1051,15 +1079,15 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
   __syncthreads();
   if (writer) {
     const int t = threadIdx.x;
-    if (t <= K) {
+    if (t <= KM) {
       int32_t tok = -1;
       if (t < a) tok = __ldg(dr + t);
       else if (t == a) tok = (int32_t)b;
-      P.out_tokens[(size_t)r * (K + 1) + t] = tok;
+      P.out_tokens[(size_t)r * (KM + 1) + t] = tok;
     }
-    if (t < K) {
-      if (P.p_at) P.p_at[(size_t)r * K + t] = sm.P[t];
-      if (P.q_at) P.q_at[(size_t)r * K + t] = sm.Q[t];
+    if (t < KM) {
+      if (P.p_at) P.p_at[(size_t)r * KM + t] = sm.P[t];
+      if (P.q_at) P.q_at[(size_t)r * KM + t] = sm.Q[t];
     }
     if (t == 0) {
       P.num_accepted[r] = a;
@@ -1213,7 +1241,8 @@ extern "C" int sd_verify_kernel_count(int B, int V, int dtype, int has_temperatu
 
 extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* target, long ld_t,
                                 const void* draft, long ld_d, const int32_t* drafts,
-                                const float* temperature, uint64_t seed, uint32_t request_base,
+                                const int32_t* cu_drafts, const float* temperature,
+                                uint64_t seed, uint32_t request_base,
                                 int32_t* out_tokens,
                                 int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
                                 void* workspace, int32_t* err, cudaStream_t stream) {
@@ -1229,6 +1258,7 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.ld_d = ld_d;
   P.drafts = drafts;
   P.temperature = temperature;
+  P.cu = cu_drafts;
   P.rk = sdk::philox_round_keys(seed);
   P.rbase = request_base;
   P.out_tokens = out_tokens;
@@ -1327,9 +1357,9 @@ extern "C" int sd_verify_noalloc_launch(int B, int K, int V, int dtype, const vo
   // no earlier call's state can leak into this one.
   if (cudaMemsetAsync(slots, 0, (size_t)B * sizeof(sdk::RaceSlot), stream) != cudaSuccess)
     return SD_E_LAUNCH;
-  return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed,
-                          request_base, out_tokens, num_accepted, p_at_draft, q_at_draft, slots,
-                          err, stream);
+  return sd_verify_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, nullptr,
+                          temperature, seed, request_base, out_tokens, num_accepted, p_at_draft,
+                          q_at_draft, slots, err, stream);
 }
 
 // Drafter-side sampling: one cluster per row (the verify kernel's cluster size for V).
