@@ -199,7 +199,7 @@ def _draft_sample(fn, rows, B, K, temperature, seed, req_ids, nthreads):
 
 
 def draft_sample_probs(q, temperature=None, seed=0, req_ids=None, nthreads=0):
-    """Drafter-side sampling on fp32 rows q [B, K, V] (reading R7)."""
+    """Drafter-side sampling on fp32 rows q [B, K, V] (reading R13)."""
     q = _c(q, np.float32)
     B, K, _ = q.shape
     return _draft_sample(_load().oracle_draft_sample_probs, q, B, K, temperature, seed, req_ids,
@@ -284,7 +284,7 @@ def pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_
 
 def pdraft_prepare_padded(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,
                           target_hidden_bits, h_shared_bits):
-    """Padded drafter batch (reading R8): B rows of 2K slots, every output row written."""
+    """Padded drafter batch (reading R14): B rows of 2K slots, every output row written."""
     out_tokens = _c(out_tokens, np.int32)
     num_accepted = _c(num_accepted, np.int32)
     pos0 = _c(pos0, np.int32)

@@ -34,11 +34,11 @@
 //  R5 drafter slot j of request r takes target hidden row r*(K+1)+j for j <= a_r, MASK slots
 //     take h_shared (map -1); positions are pos0 + 1 + j.
 //  R6 is_rejected is over the verify batch [B, K+1]: 1 for draft slots j > a_r, 0 for slot 0.
-//  R7 drafter-side sampling (the drafter's K outputs per request become the next step's drafts):
+//  R13 drafter-side sampling (the drafter's K outputs per request become the next step's drafts):
 //     draft k of request r is the exponential race argmax_x q(x)/E_x over the drafter's row k,
 //     with E from word (x & 3) of block (x >> 2, k, r, 2) (tag 2, a stream of its own), the
 //     R2/R3 rules otherwise; temperature 0 takes argmax q, lowest index on ties.
-//  R8 padded drafter batch ([PE] "Hidden State 管理": rejected tokens get PADDING_SLOT_ID; the
+//  R14 padded drafter batch ([PE] "Hidden State 管理": rejected tokens get PADDING_SLOT_ID; the
 //     target hidden states are scattered to their drafter rows): request r owns the fixed row of
 //     W = 2K slots [r*W, (r+1)*W). Slots j < a_r + K are those of the packed layout (R5);
 //     slots j >= a_r + K are rejected leftovers: token mask_token_id, position pos0 + 1 + j,
@@ -107,7 +107,7 @@ double accept_uniform(uint64_t seed, uint32_t r, uint32_t j) {
 }
 
 // R1/R2: the exponential variate E_x of vocab entry x on row j of request r (tag 1: the verify
-// races; tag 2: drafter-side sampling, R7).
+// races; tag 2: drafter-side sampling, R13).
 float race_E(uint64_t seed, uint32_t r, uint32_t j, uint32_t x, uint32_t tag = 1u) {
   const uint32_t w = philox_word(seed, x >> 2, j, r, tag, (int)(x & 3u));
   const double v = ((double)w + 0.5) * (1.0 / 4294967296.0);
@@ -512,7 +512,7 @@ int oracle_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t*
   return 0;
 }
 
-// Padded drafter batch (R8) with its hidden states: every one of the B*2K rows is written.
+// Padded drafter batch (R14) with its hidden states: every one of the B*2K rows is written.
 int oracle_pdraft_prepare_padded(int B, int K, const int32_t* out_tokens,
                                  const int32_t* num_accepted, const int32_t* pos0,
                                  const int32_t* block_table, int max_blocks, int block_size,
@@ -596,7 +596,7 @@ int oracle_hidden_gather(int capacity, int H, const int32_t* total_out, const in
   return 0;
 }
 
-// Drafter-side sampling (R7) on fp32 probability rows: row (i*K + k) at q + row*ld is the
+// Drafter-side sampling (R13) on fp32 probability rows: row (i*K + k) at q + row*ld is the
 // drafter's distribution for draft k of request i. Keys q(x)/E_x are fp32 divisions (R3), the
 // largest wins, lowest x on ties; T == 0 takes the argmax. A row without a positive key gives
 // token 0 and ERR_ZERO_ROW. margin (nullable) [B*K] receives (k1 - k2) / k1.
@@ -646,7 +646,7 @@ int oracle_draft_sample_probs(int B, int K, int V, const float* q, long ld,
   return 0;
 }
 
-// Drafter-side sampling (R7) on bf16 logit rows: q = softmax(l / T) in double, keys q/E in
+// Drafter-side sampling (R13) on bf16 logit rows: q = softmax(l / T) in double, keys q/E in
 // double; T == 0 takes the argmax of the raw logits.
 int oracle_draft_sample_logits(int B, int K, int V, const uint16_t* logits, long ld,
                                const float* temperature, uint64_t seed, const int32_t* req_ids,

@@ -1,4 +1,4 @@
-"""Pins of the oracle's drafter-side sampling (reading R7: the drafter's K output rows per request
+"""Pins of the oracle's drafter-side sampling (reading R13: the drafter's K output rows per request
 are sampled by the exponential race with the Philox tag-2 stream; temperature 0 takes the argmax).
 
 What the mathematics fixes: the race argmax_x q(x)/E_x with E_x ~ Exp(1) independent draws x

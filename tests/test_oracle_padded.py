@@ -1,4 +1,4 @@
-"""Pins of the oracle's padded drafter batch (reading R8 of the P-EAGLE blog's rebuild: fixed rows
+"""Pins of the oracle's padded drafter batch (reading R14 of the P-EAGLE blog's rebuild: fixed rows
 of 2K slots per request, rejected leftovers on PADDING_SLOT_ID = -1, scatter-form hidden map).
 
 A hand-worked example (tests/golden/padded_hand_example.json), then invariants against the
