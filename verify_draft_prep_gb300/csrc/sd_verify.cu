@@ -532,6 +532,166 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
   return block_max_u64<NT>(best, sm.red);
 }
 
+// ------------------------------------------------------------- log-domain race on logit rows
+// For a race on softmax(l c ln2) itself (the drafter-side sampler), the winner
+// argmax_x q(x)/E_x equals argmax_x (l_x c - log2 E_x): the softmax's maximum and normaliser are
+// common factors, so one pass over the row suffices. The filter key is
+// beta_x = l_x c - lg2(L_x), with L_x ~= -log2 v_x = E_x log2(e) from the hardware lg2 (the series
+// near v = 1, as for R); it differs from the exact log key by the constant log2(log2 e) and an
+// error below 2.5e-4 (L's measured relative error 1.669e-4 times log2 e, plus fp32 rounding of
+// l c), far inside kLogBand, the band log2(1 + 2^-7) of the linear filter. Exact keys, for
+// candidate units only: l_x c - log2(E_x) in double with E_x exactly as the verify race's,
+// rounded to fp32 and packed as an orderable float (a tie within one fp32 step of the key goes
+// to the lowest x).
+constexpr float kLogBand = 0.01122f;   // log2(1 + 2^-7)
+constexpr float kLogSlack = 0.002f;    // approximation allowance inside the per-unit bound
+
+__device__ __forceinline__ float race_L(uint32_t w) {  // ~ -log2 v, v = (w + 0.5) 2^-32
+  if (w < kNearOne) return -fast_lg2(fmaf(__uint2float_rn(w), 0x1p-32f, 0x1p-33f));
+  const float m = fmaf(__uint2float_rn(~w), 0x1p-32f, 0x1p-33f);  // 1 - v
+  return (m * fmaf(m, fmaf(m, 0.33333334f, 0.5f), 1.0f)) * kLog2e;
+}
+
+__device__ __forceinline__ uint64_t log_exact_key(float l, float c, uint32_t w, uint32_t x) {
+  const double key = (double)l * (double)c - log2((double)race_E_exact(w));
+  return pack_key(orderable((float)key), x);
+}
+
+__device__ __noinline__ void log_exact_unit(const uint16_t* row, uint32_t V, bool vec, float c,
+                                            uint32_t u, const PhiloxRoundKeys& rk, uint32_t rid,
+                                            uint32_t j, uint32_t tag, uint64_t& best) {
+  const uint4 raw = bf16_raw(row, u, V, vec);
+  uint4 w[2];
+  w[0] = race_block(rk, 2u * u, rid, j, tag);
+  w[1] = race_block(rk, 2u * u + 1u, rid, j, tag);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float l = bf16_at(raw, e);
+    if (u * 8u + e < V && l > -INFINITY) {
+      const uint64_t k = log_exact_key(l, c, word_of(w[e >> 2], e & 3), u * 8u + e);
+      best = k > best ? k : best;
+    }
+  }
+}
+
+// Largest filter key of one unit (-inf when every logit is -inf).
+__device__ __forceinline__ float log_unit_max(const uint4& raw, const uint4 (&w)[2], float c) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    m = fmaxf(m, fmaf(bf16_at(raw, e), c, -fast_lg2(race_L(word_of(w[e >> 2], e & 3)))));
+  return m;
+}
+
+// One unit of the log-domain pass; *tau holds the CTA's running best (orderable bits, 0 = none).
+__device__ __forceinline__ void log_take(const uint4& raw, const uint4 (&w)[2], float c,
+                                         uint32_t u, float& a1, float& a2, uint32_t& best_u,
+                                         uint32_t* tau) {
+  uint32_t m01, m23, mm;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m01) : "r"(raw.x), "r"(raw.y));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(m23) : "r"(raw.z), "r"(raw.w));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(mm) : "r"(m01), "r"(m23));
+  const float lmax = fmaxf(__uint_as_float(mm << 16), __uint_as_float(mm & 0xffff0000u));
+  const uint32_t wmax = unit_wmax<8>(w);
+  const uint32_t tb = *(volatile uint32_t*)tau;
+  const float shared_best = tb ? __uint_as_float(tb & 0x80000000u ? tb & 0x7fffffffu : ~tb)
+                               : -INFINITY;
+  const float thr = fmaxf(a1, shared_best);
+  // bound of every beta_x of the unit: the largest logit and the largest word (L falls with w)
+  if (fmaf(lmax, c, -fast_lg2(race_L(wmax))) + kLogSlack < thr - kLogBand) return;
+  const float m = log_unit_max(raw, w, c);
+  a2 = fmaxf(a2, fminf(m, a1));
+  best_u = m > a1 ? u : best_u;
+  if (m > thr) atomicMax(tau, orderable(m));
+  a1 = fmaxf(a1, m);
+}
+
+// The exact log-domain race winner over units [u0, u1) of one logit row: the CTA's packed
+// (orderable key, ~x) maximum, or 0 when every logit of the share is -inf.
+__device__ uint64_t race_chunk_log(const uint16_t* row, uint32_t V, bool vec, float c,
+                                   uint32_t u0, uint32_t u1, const PhiloxRoundKeys& rk,
+                                   uint32_t rid, uint32_t j, uint32_t tag, Smem& sm) {
+  float a1 = -INFINITY, a2 = -INFINITY;
+  uint32_t best_u = 0xffffffffu;
+  const uint32_t uf = vec ? max(u0, min(u1, V / 8u)) : u0;
+  uint32_t ub = u0 + threadIdx.x;
+  constexpr int UNR = 2;
+  if (ub + (UNR - 1) * NT < uf) {
+    uint4 raw[UNR];
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) raw[k] = ld_stream_u4(row + 8u * (ub + k * NT));
+    for (; ub + (2 * UNR - 1) * NT < uf; ub += UNR * NT) {
+#pragma unroll
+      for (int k = 0; k < UNR; ++k) {
+        const uint32_t u = ub + k * NT;
+        uint4 w[2];
+        w[0] = race_block(rk, 2u * u, rid, j, tag);
+        w[1] = race_block(rk, 2u * u + 1u, rid, j, tag);
+        log_take(raw[k], w, c, u, a1, a2, best_u, &sm.tau);
+        raw[k] = ld_stream_u4(row + 8u * (u + UNR * NT));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < UNR; ++k) {
+      const uint32_t u = ub + k * NT;
+      uint4 w[2];
+      w[0] = race_block(rk, 2u * u, rid, j, tag);
+      w[1] = race_block(rk, 2u * u + 1u, rid, j, tag);
+      log_take(raw[k], w, c, u, a1, a2, best_u, &sm.tau);
+    }
+    ub += UNR * NT;
+  }
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked (-inf past the row end)
+    const uint4 raw = bf16_raw(row, ub, V, vec);
+    uint4 w[2];
+    w[0] = race_block(rk, 2u * ub, rid, j, tag);
+    w[1] = race_block(rk, 2u * ub + 1u, rid, j, tag);
+    log_take(raw, w, c, ub, a1, a2, best_u, &sm.tau);
+  }
+  if (threadIdx.x == 0) sm.ncand = 0;
+  const uint32_t Ab = (uint32_t)block_max_u64<NT>(a1 > -INFINITY ? orderable(a1) : 0u, sm.red);
+  if (threadIdx.x == 0) sm.tau = 0u;  // every thread has left the streaming pass
+  uint64_t best = 0ull;
+  if (Ab != 0u) {
+    const float A = __uint_as_float(Ab & 0x80000000u ? Ab & 0x7fffffffu : ~Ab);
+    bool rescan = a2 >= A - kLogBand;
+    if (!rescan && a1 >= A - kLogBand) {
+      const int slot = atomicAdd(&sm.ncand, 1);
+      if (slot < kCandCap) sm.cand[slot] = best_u;
+      else rescan = true;
+    }
+    if (rescan) {  // this thread's other units may hold candidates too (rare)
+      for (uint32_t u = u0 + threadIdx.x; u < u1; u += NT) {
+        const uint4 raw = bf16_raw(row, u, V, vec);
+        uint4 w[2];
+        w[0] = race_block(rk, 2u * u, rid, j, tag);
+        w[1] = race_block(rk, 2u * u + 1u, rid, j, tag);
+        if (log_unit_max(raw, w, c) >= A - kLogBand)
+          log_exact_unit(row, V, vec, c, u, rk, rid, j, tag, best);
+      }
+    }
+    __syncthreads();
+    const int nc = min(sm.ncand, kCandCap);
+    if (threadIdx.x < 32) {
+      for (int base = 0; base < nc * 8; base += 32) {
+        const int l = base + (int)threadIdx.x;
+        if (l < nc * 8) {
+          const uint32_t x = sm.cand[l / 8] * 8u + (uint32_t)(l % 8);
+          if (x < V) {
+            const float lv = bf16_bits_to_float(__ldg(row + x));
+            if (lv > -INFINITY) {
+              const uint4 w4 = race_block(rk, x >> 2, rid, j, tag);
+              const uint64_t k = log_exact_key(lv, c, word_of(w4, x & 3u), x);
+              best = k > best ? k : best;
+            }
+          }
+        }
+      }
+    }
+  }
+  return block_max_u64<NT>(best, sm.red);
+}
+
 // --------------------------------------------------------------------------------- greedy rows
 __device__ __forceinline__ void argmax_take(float v, uint32_t x, float& best, uint32_t& bx) {
   if (v > best) {
@@ -1161,13 +1321,12 @@ __global__ void __launch_bounds__(NT, kMinBlocks) sample_kernel(const __grid_con
     pk = cluster_max_u64(race_chunk(src, u0, u1, P.rk, rid, (uint32_t)k, sm, kTagDraft), sm,
                          phase, cl);
   } else {
+    // one pass: the log-domain race needs no softmax statistics
     const uint16_t* rp = (const uint16_t*)P.rows + (size_t)row * P.ld;
     const float c = 1.4426950408889634f / T;
-    MaxSum st, unused;
-    row_stats<false>(rp, nullptr, V, vec, u0, u1, c, st, unused, sm, phase, cl);
-    Bf16Residual<false> src{rp, nullptr, st.m, 1.0f / st.s, 0.0f, 0.0f, c, V, vec};
-    pk = cluster_max_u64(race_chunk(src, u0, u1, P.rk, rid, (uint32_t)k, sm, kTagDraft), sm,
-                         phase, cl);
+    pk = cluster_max_u64(race_chunk_log(rp, V, vec, c, u0, u1, P.rk, rid, (uint32_t)k, kTagDraft,
+                                        sm),
+                         sm, phase, cl);
   }
   uint32_t b = 0;
   if (T == 0.0f) {
