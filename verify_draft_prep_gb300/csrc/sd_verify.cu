@@ -309,6 +309,9 @@ struct Smem {
   uint64_t red[NT / 32];
   float redf[4][NT / 32];
   uint64_t slot[2];   // per-CTA cluster exchange (double-buffered)
+  uint64_t slot2[2];  // second value of a paired exchange (greedy rows two at a time)
+  uint64_t red2[NT / 32];
+  uint64_t bcast2;
   float4 fslot[2];
   uint64_t bcast;
   float4 fbcast;
@@ -340,6 +343,36 @@ __device__ uint64_t cluster_max_u64(uint64_t v, Smem& sm, int& phase, int cl) {
   const uint64_t m = sm.bcast;
   phase ^= 1;
   return m;
+}
+
+// The same for two values at once: one cluster barrier for both.
+__device__ void cluster_max2_u64(uint64_t& v0, uint64_t& v1, Smem& sm, int& phase, int cl) {
+  if (cl == 1) return;
+  if (threadIdx.x == 0) {
+    sm.slot[phase] = v0;
+    sm.slot2[phase] = v1;
+  }
+  cluster_barrier();
+  if (threadIdx.x < 32) {
+    const bool in = threadIdx.x < (unsigned)cl;
+    uint64_t m0 = in ? load_from_rank(&sm.slot[phase], threadIdx.x) : 0ull;
+    uint64_t m1 = in ? load_from_rank(&sm.slot2[phase], threadIdx.x) : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t x0 = __shfl_xor_sync(0xffffffffu, m0, o);
+      const uint64_t x1 = __shfl_xor_sync(0xffffffffu, m1, o);
+      m0 = x0 > m0 ? x0 : m0;
+      m1 = x1 > m1 ? x1 : m1;
+    }
+    if (threadIdx.x == 0) {
+      sm.bcast = m0;
+      sm.bcast2 = m1;
+    }
+  }
+  __syncthreads();
+  v0 = sm.bcast;
+  v1 = sm.bcast2;
+  phase ^= 1;
 }
 
 // ------------------------------------------------------------------------------------ the race
@@ -752,6 +785,102 @@ __device__ uint64_t argmax_chunk(const void* row, uint32_t V, bool vec, uint32_t
   return block_max_u64<NT>(pk, sm.red);
 }
 
+// Argmax of two rows at once over units [u0, u1) (greedy rows j and j+1): both rows' loads in
+// flight together, the two block maxima in one reduction.
+template <int DT>
+__device__ void argmax_chunk2(const void* row0, const void* row1, uint32_t V, bool vec,
+                              uint32_t u0, uint32_t u1, Smem& sm, uint64_t& pk0, uint64_t& pk1) {
+  constexpr int EPU = DT == SD_F32_PROBS ? 4 : 8;
+  constexpr int U = kArgmaxUnroll / 2;  // units in flight per row
+  float best0 = -INFINITY, best1 = -INFINITY;
+  uint32_t bx0 = 0xffffffffu, bx1 = 0xffffffffu;
+  const uint32_t uf = vec ? max(u0, min(u1, V / EPU)) : u0;
+  uint32_t ub = u0 + threadIdx.x;
+  auto take = [&](const uint4& v, uint32_t u, float& best, uint32_t& bx) {
+    const uint32_t x0 = u * EPU;
+    if (DT == SD_F32_PROBS) {
+      argmax_take(__uint_as_float(v.x), x0 + 0, best, bx);
+      argmax_take(__uint_as_float(v.y), x0 + 1, best, bx);
+      argmax_take(__uint_as_float(v.z), x0 + 2, best, bx);
+      argmax_take(__uint_as_float(v.w), x0 + 3, best, bx);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) argmax_take(bf16_at(v, i), x0 + i, best, bx);
+    }
+  };
+  auto load = [&](const void* row, uint32_t u) {
+    return ld_stream_u4((const char*)row + (size_t)u * 16u);
+  };
+  if (ub + (U - 1) * NT < uf) {  // unchecked 128-bit loads, U units of each row in flight
+    uint4 v0[U], v1[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      v0[k] = load(row0, ub + k * NT);
+      v1[k] = load(row1, ub + k * NT);
+    }
+    for (; ub + (2 * U - 1) * NT < uf; ub += U * NT) {
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        take(v0[k], ub + k * NT, best0, bx0);
+        take(v1[k], ub + k * NT, best1, bx1);
+        v0[k] = load(row0, ub + (k + U) * NT);
+        v1[k] = load(row1, ub + (k + U) * NT);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      take(v0[k], ub + k * NT, best0, bx0);
+      take(v1[k], ub + k * NT, best1, bx1);
+    }
+    ub += U * NT;
+  }
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked
+    if (DT == SD_F32_PROBS) {
+      float a[4], b[4];
+      f32_unit((const float*)row0, ub, V, vec, -INFINITY, a);
+      f32_unit((const float*)row1, ub, V, vec, -INFINITY, b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        argmax_take(a[i], ub * 4 + i, best0, bx0);
+        argmax_take(b[i], ub * 4 + i, best1, bx1);
+      }
+    } else {
+      const uint4 a = bf16_raw((const uint16_t*)row0, ub, V, vec);
+      const uint4 b = bf16_raw((const uint16_t*)row1, ub, V, vec);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        argmax_take(bf16_at(a, i), ub * 8 + i, best0, bx0);
+        argmax_take(bf16_at(b, i), ub * 8 + i, best1, bx1);
+      }
+    }
+  }
+  uint64_t p0 = (bx0 == 0xffffffffu) ? 0ull : pack_key(orderable(best0), bx0);
+  uint64_t p1 = (bx1 == 0xffffffffu) ? 0ull : pack_key(orderable(best1), bx1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t x0 = __shfl_xor_sync(0xffffffffu, p0, o);
+    const uint64_t x1 = __shfl_xor_sync(0xffffffffu, p1, o);
+    p0 = x0 > p0 ? x0 : p0;
+    p1 = x1 > p1 ? x1 : p1;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) {
+    sm.red[warp] = p0;
+    sm.red2[warp] = p1;
+  }
+  __syncthreads();
+  p0 = 0ull;
+  p1 = 0ull;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    p0 = sm.red[w] > p0 ? sm.red[w] : p0;
+    p1 = sm.red2[w] > p1 ? sm.red2[w] : p1;
+  }
+  pk0 = p0;
+  pk1 = p1;
+}
+
 // ------------------------------------------------------------------- softmax statistics (bf16)
 struct MaxSum {
   float m, s;
@@ -1099,36 +1228,50 @@ __global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_con
   __syncthreads();
 
   if (greedy) {
-    // ---- temperature 0: accept while the draft is the row's argmax (lowest index on ties)
-    for (int j = 0; j <= K; ++j) {
-      const uint64_t pk =
-          cluster_max_u64(argmax_chunk<DT>(trow(j), V, vec, u0, u1, sm), sm, phase, cl);
-      const uint32_t am = pk ? packed_index(pk) : 0u;  // no value above -inf: entry 0
-      if (j == K) {
-        b = am;
-        break;
+    // ---- temperature 0: accept while the draft is the row's argmax (lowest index on ties).
+    // Rows go two at a time (j, j+1): one pass and one cluster exchange per pair, at the cost
+    // of reading row j+1 for nothing when draft j is rejected.
+    bool done = false;
+    for (int j0 = 0; j0 <= K && !done; j0 += 2) {
+      uint64_t pks[2];
+      if (j0 + 1 <= K) {
+        argmax_chunk2<DT>(trow(j0), trow(j0 + 1), V, vec, u0, u1, sm, pks[0], pks[1]);
+        cluster_max2_u64(pks[0], pks[1], sm, phase, cl);
+      } else {
+        pks[0] = cluster_max_u64(argmax_chunk<DT>(trow(j0), V, vec, u0, u1, sm), sm, phase, cl);
+        pks[1] = 0ull;
       }
-      const int d = __ldg(dr + j);
-      const bool valid = d >= 0 && (uint32_t)d < V;
-      if (threadIdx.x == 0) {
-        if (valid) {
-          if (DT == SD_F32_PROBS) {
-            sm.P[j] = __ldg((const float*)trow(j) + d);
-            sm.Q[j] = __ldg((const float*)drow(j) + d);
-          } else {
-            sm.P[j] = bf16_bits_to_float(__ldg((const uint16_t*)trow(j) + d));
-            sm.Q[j] = bf16_bits_to_float(__ldg((const uint16_t*)drow(j) + d));
-          }
-        } else {
-          sm.P[j] = 0.0f;
-          sm.Q[j] = 0.0f;
+      for (int t = 0; t < 2 && !done; ++t) {
+        const int j = j0 + t;
+        const uint64_t pk = pks[t];
+        const uint32_t am = pk ? packed_index(pk) : 0u;  // no value above -inf: entry 0
+        if (j == K) {
+          b = am;
+          done = true;
+          break;
         }
-      }
-      if (!valid) e |= SD_ERR_TOKEN_RANGE;
-      if (!valid || (uint32_t)d != am) {
-        a = j;
-        b = am;
-        break;
+        const int d = __ldg(dr + j);
+        const bool valid = d >= 0 && (uint32_t)d < V;
+        if (threadIdx.x == 0) {
+          if (valid) {
+            if (DT == SD_F32_PROBS) {
+              sm.P[j] = __ldg((const float*)trow(j) + d);
+              sm.Q[j] = __ldg((const float*)drow(j) + d);
+            } else {
+              sm.P[j] = bf16_bits_to_float(__ldg((const uint16_t*)trow(j) + d));
+              sm.Q[j] = bf16_bits_to_float(__ldg((const uint16_t*)drow(j) + d));
+            }
+          } else {
+            sm.P[j] = 0.0f;
+            sm.Q[j] = 0.0f;
+          }
+        }
+        if (!valid) e |= SD_ERR_TOKEN_RANGE;
+        if (!valid || (uint32_t)d != am) {
+          a = j;
+          b = am;
+          done = true;
+        }
       }
     }
   } else if (DT == SD_F32_PROBS) {
