@@ -38,10 +38,10 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "063107533b338996"): (82.450944e6, "ncu --set full, one launch of the full batch"),
-    ("b256mix", "063107533b338996"): (401.228288e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "063107533b338996"): (785.44e6, "ncu --set full at B=160, scaled x3.2"),
-    ("b1024lg", "063107533b338996"): (3055.43e6, "ncu --set full at B=96, scaled x1024/96"),
+    ("b64", "a10a92db30eb38db"): (82.316288e6, "ncu --set full, one launch of the full batch"),
+    ("b256mix", "a10a92db30eb38db"): (439.077376e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "a10a92db30eb38db"): (783.758944e6, "ncu --set full at B=160, scaled x3.2"),
+    ("b1024lg", "a10a92db30eb38db"): (3025.6142e6, "ncu --set full at B=96, scaled x1024/96"),
 }
 
 
