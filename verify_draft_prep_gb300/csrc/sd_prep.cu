@@ -58,6 +58,22 @@ struct PrepParams {
   int32_t* err;
 };
 
+// One warp copies a row of nv 16-byte words: each lane issues all of its loads (up to
+// kCopyBatch) before its stores, so a row of a few KB costs one memory round trip.
+constexpr int kCopyBatch = 12;
+__device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src,
+                                              uint4* __restrict__ dst, int nv, int lane) {
+  for (int v0 = lane; v0 < nv; v0 += 32 * kCopyBatch) {
+    uint4 x[kCopyBatch];
+#pragma unroll
+    for (int k = 0; k < kCopyBatch; ++k)
+      if (v0 + 32 * k < nv) x[k] = __ldg(src + v0 + 32 * k);
+#pragma unroll
+    for (int k = 0; k < kCopyBatch; ++k)
+      if (v0 + 32 * k < nv) dst[v0 + 32 * k] = x[k];
+  }
+}
+
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -233,16 +249,7 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
         const int nv = P.H >> 3;
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(dst);
-        int v = lane;
-        for (; v + 96 < nv; v += 128) {
-          const uint4 x0 = __ldg(s4 + v), x1 = __ldg(s4 + v + 32), x2 = __ldg(s4 + v + 64),
-                      x3 = __ldg(s4 + v + 96);
-          d4[v] = x0;
-          d4[v + 32] = x1;
-          d4[v + 64] = x2;
-          d4[v + 96] = x3;
-        }
-        for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
+        copy_row_warp(s4, d4, nv, lane);
       } else {
         for (int x = lane; x < P.H; x += 32) dst[x] = __ldg(src + x);
       }
@@ -343,16 +350,7 @@ __global__ void __launch_bounds__(PNT) prep_padded_kernel(const PaddedParams P) 
         const int nv = P.H >> 3;
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(dst);
-        int v = lane;
-        for (; v + 96 < nv; v += 128) {
-          const uint4 x0 = __ldg(s4 + v), x1 = __ldg(s4 + v + 32), x2 = __ldg(s4 + v + 64),
-                      x3 = __ldg(s4 + v + 96);
-          d4[v] = x0;
-          d4[v + 32] = x1;
-          d4[v + 64] = x2;
-          d4[v + 96] = x3;
-        }
-        for (; v < nv; v += 32) d4[v] = __ldg(s4 + v);
+        copy_row_warp(s4, d4, nv, lane);
       } else {
         for (int x = lane; x < P.H; x += 32) dst[x] = __ldg(src + x);
       }
