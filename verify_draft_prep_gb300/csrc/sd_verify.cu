@@ -40,6 +40,11 @@ constexpr int UNROLL = 4;      // 16-byte units in flight per thread (greedy row
 constexpr int kArgmaxUnroll = 8;  // the same for greedy argmax rows (loads only: more in flight)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
 constexpr int kMinBlocks = 4;  // resident CTAs per SM the cluster kernel's registers allow
+// the verify kernel on fp32 rows keeps 2 race units in flight per thread and fits 5 CTAs per SM
+// (measured better than 4 CTAs with 4 units for the one-wave and mixed batches); on logit rows
+// the statistics pass needs the registers of 4
+constexpr int kMinBlocksF32 = 5;
+constexpr int min_blocks(int dt) { return dt == SD_F32_PROBS ? kMinBlocksF32 : kMinBlocks; }
 constexpr int kRaceMinBlocks = 4;  // the same for race_kernel (its loop keeps 3 units in flight)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
 constexpr int kCandCap = 32;            // candidate units evaluated lane-parallel per CTA
@@ -144,7 +149,7 @@ __device__ __forceinline__ float bf16_at(const uint4& w, int i) {
 template <bool HAS_Q>
 struct F32Residual {
   static constexpr int EPU = 4;
-  static constexpr int UNR = 4;  // units in flight per thread
+  static constexpr int UNR = 2;  // units in flight per thread
   static constexpr int ROWS = HAS_Q ? 2 : 1;
   const float* p;
   const float* q;
@@ -1180,7 +1185,8 @@ __device__ __forceinline__ void race_role(const VerifyParams& P, uint32_t c, Sme
 
 // ---------------------------------------------------------------------------------- the kernel
 template <int DT>
-__global__ void __launch_bounds__(NT, kMinBlocks) verify_kernel(const __grid_constant__ VerifyParams P) {
+__global__ void __launch_bounds__(NT, min_blocks(DT))
+    verify_kernel(const __grid_constant__ VerifyParams P) {
   __shared__ Smem sm;
   constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
   using Elt = typename std::conditional<DT == SD_F32_PROBS, float, uint16_t>::type;
@@ -1527,7 +1533,7 @@ int choose_cluster(int V, int epu) {
 static int race_grid(int B, int V, int dtype, bool has_temperature, int nc) {
   if (dtype != SD_F32_PROBS || (V + 3) / 4 < 2048 || has_temperature) return 0;
   const int sms = sm_count();
-  if ((long)B * nc < 2L * sdk::kMinBlocks * sms) return 0;  // measured faster in clusters
+  if ((long)B * nc < 2L * sdk::kMinBlocksF32 * sms) return 0;  // measured faster per request
   long g = (long)sdk::kRaceMinBlocks * sms;
   // a CTA's share spans at most B/g + 2 requests: g >= B/6 keeps that within kMaxSeg
   if (g < (B + 5) / 6) g = (B + 5) / 6;
@@ -1574,9 +1580,9 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.race_blocks = race_grid(B, V, dtype, temperature != nullptr, P.nc);
   if (P.race_blocks == 0 && dtype == SD_F32_PROBS && temperature == nullptr) {
     // every request samples: its CTAs exchange nothing through shared memory, so no cluster is
-    // needed, and each row splits over as many CTAs as fill one wave of kMinBlocks per SM
+    // needed, and each row splits over as many CTAs as fill one wave of kMinBlocksF32 per SM
     const int nu = (V + 3) / 4;
-    int nc = sdk::kMinBlocks * sm_count() / std::max(B, 1);
+    int nc = sdk::kMinBlocksF32 * sm_count() / std::max(B, 1);
     nc = std::min(nc, std::max(1, nu / (2 * sdk::NT)));
     P.cl = 1;
     P.nc = std::max(nc, 1);
