@@ -6,23 +6,31 @@
 // draft is accepted; section "边界与代价": temperature 0 must reproduce greedy decoding.
 //
 // Design (one GB300, HBM-bound):
-//  * One thread-block cluster of CL CTAs per request. Each CTA owns 1/CL of every vocab row; the
-//    CTAs combine row-wide results (argmax keys, softmax statistics) through distributed shared
-//    memory, so a request's rows are visited in order and nothing is read past the first
-//    rejection. No global workspace, no atomics on the data path, no spin-waits.
+//  * Greedy and logit requests: one thread-block cluster of CL CTAs per request. Each CTA owns
+//    1/CL of every vocab row; the CTAs combine row-wide results (argmax keys, softmax
+//    statistics) through distributed shared memory, so a request's rows are visited in order and
+//    nothing is read past the first rejection (greedy rows two at a time, at the cost of one
+//    speculative row). No spin-waits.
 //  * Sampled requests on probability rows: the accept scan is K scalar gathers (one lane per
-//    draft); only the one residual (or bonus) row pair is streamed, with 128-bit loads.
+//    draft); only the one residual (or bonus) row pair is streamed, with 128-bit loads, split
+//    over the request's CTAs (no cluster needed when no request is greedy), which merge their
+//    exact best through a 16-byte slot per request (atomicMax of the packed key, a unit count).
+//    Batches that fill the GPU twice or more go to race_kernel, which splits all race rows
+//    evenly over a whole number of CTAs per SM and runs each CTA's few accept scans first.
 //  * The residual resample is an exponential race argmax_x r(x)/E_x. E_x needs a double log,
 //    which GB300 executes slowly, so each thread filters with an fp32 approximation (one
 //    hardware lg2) and keeps only elements whose approximate key lies within a relative band
 //    of its running best; the CTA then evaluates the exact key r / fp32(-log(v)) for the few
 //    candidates. The band is 16x the exhaustively measured worst error of the approximation,
 //    so the winner (including the lowest-index rule on exact ties) is always among the
-//    candidates.
-//  * Greedy requests scan rows 0..a_r in order, one cluster-wide argmax per row.
+//    candidates. A per-unit upper bound against the CTA's running best skips units that cannot
+//    hold a candidate.
 //  * Logit rows (bf16): per row the cluster forms max and sum of exp2((l - M) * log2(e)/T) for
 //    the target and draft rows together, decides the draft, and on rejection races on the same
 //    rows again (the second read is served from L2).
+//  * Per-request draft counts (a prefix of the counts) address each request's packed rows; the
+//    drafter-side sampler (sample_kernel) races each drafter row on its own Philox stream, in the
+//    log domain for logit rows (one pass: the softmax normaliser cancels).
 
 #include <float.h>
 #include <math.h>
@@ -162,10 +170,6 @@ struct F32Residual {
     f32_unit(p, u, V, vec, 0.0f, raw.p);
     if (HAS_Q) f32_unit(q, u, V, vec, 0.0f, raw.q);
   }
-  __device__ __forceinline__ void zero(Raw& raw) const {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) raw.p[i] = raw.q[i] = 0.0f;
-  }
   // units entirely inside the row, read with unchecked 128-bit loads when vec is set
   __device__ __forceinline__ uint32_t full_units() const { return V / 4u; }
   __device__ __forceinline__ const uint8_t* row_bytes(int r) const {
@@ -268,9 +272,6 @@ struct Bf16Residual {
   __device__ __forceinline__ void fetch(uint32_t u, Raw& raw) const {
     raw.t = bf16_raw(t, u, V, vec);
     if (HAS_Q) raw.d = bf16_raw(d, u, V, vec);
-  }
-  __device__ __forceinline__ void zero(Raw& raw) const {
-    raw.t = raw.d = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   }
   __device__ __forceinline__ uint32_t full_units() const { return V / 8u; }
   __device__ __forceinline__ const uint8_t* row_bytes(int r) const {
