@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   // inputs not written by sd_verify
   for (int q = tid; q < nreq; q += PNT) s_pos[q] = __ldg(P.pos0 + r0 + q);
   grid_dependency_wait();
+  // A programmatically dependent launch (the next kernel on the stream, e.g. the next step's
+  // verify) may be scheduled from here on: this grid is small, and the dependent waits for this
+  // grid's completion (griddepcontrol.wait) before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // this CTA's first PNT accepted counts, loaded together with the prefix's (one round trip)
   const int a_first = tid < nreq ? P.num_accepted[r0 + tid] : 0;
@@ -256,9 +260,6 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
     }
   }
 
-  // a programmatically dependent launch (the next step's verify) may now be scheduled; it
-  // waits for this grid's completion before it reads anything
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (e) atomicOr(&s_err, e);
   __syncthreads();
   if (tid == 0) raise_err(P.err, s_err);
@@ -309,6 +310,7 @@ __global__ void __launch_bounds__(PNT) prep_padded_kernel(const PaddedParams P) 
   const int r = active ? (int)(row / W) : 0, j = active ? (int)(row - (long long)r * W) : 0;
   const int p0 = active ? __ldg(P.pos0 + r) : 0;  // not written by sd_verify
   grid_dependency_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in prep_kernel
   __syncthreads();
   int32_t e = 0;
   if (active) {
@@ -356,7 +358,6 @@ __global__ void __launch_bounds__(PNT) prep_padded_kernel(const PaddedParams P) 
       }
     }
   }
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (e) atomicOr(&s_err, e);
   __syncthreads();
   if (threadIdx.x == 0) raise_err(P.err, s_err);
