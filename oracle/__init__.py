@@ -31,6 +31,7 @@ ERR_NUM_ACCEPTED = 4
 ERR_MAP_RANGE = 8
 ERR_ZERO_ROW = 16
 ERR_TOTAL_RANGE = 32
+ERR_DRAFT_COUNT = 128
 
 
 def build(force: bool = False) -> str:
@@ -77,7 +78,7 @@ def _load():
         lib.oracle_verify_logits.argtypes = verify_args
         lib.oracle_verify_logits.restype = i32
         lib.oracle_pdraft_expand.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32,
-                                             i32, P, P, P, P, P, P, P, P, P, P]
+                                             i32, P, P, P, P, P, P, P, P, P, P, P]
         lib.oracle_pdraft_expand.restype = i32
         lib.oracle_pdraft_prepare_padded.argtypes = [i32, i32, P, P, P, P, i32, i32,
                                                      ctypes.c_int32, P, P, P, P, P, P, P, P,
@@ -256,7 +257,8 @@ def verify_ragged(target, draft, drafts, cu, K_max, temperature=None, seed=0, lo
 
 
 def pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_token_id,
-                  capacity=None):
+                  capacity=None, cu=None):
+    """Drafter-batch rebuild; cu (optional [B+1]): per-request draft counts (reading R17)."""
     out_tokens = _c(out_tokens, np.int32)
     num_accepted = _c(num_accepted, np.int32)
     pos0 = _c(pos0, np.int32)
@@ -275,7 +277,8 @@ def pdraft_expand(out_tokens, num_accepted, pos0, block_table, block_size, mask_
         block_table.shape[1] if block_table.ndim == 2 else 0, block_size, mask_token_id, cap,
         _ptr(o["input_ids"]), _ptr(o["positions"]), _ptr(o["slot_mapping"]),
         _ptr(o["hidden_map"]), _ptr(o["is_masked"]), _ptr(o["is_rejected"]),
-        _ptr(o["start_loc"]), _ptr(o["new_token_idx"]), _ptr(o["total_out"]), _ptr(err))
+        _ptr(o["start_loc"]), _ptr(o["new_token_idx"]), _ptr(o["total_out"]), _ptr(err),
+        _ptr(None if cu is None else _c(cu, np.int32)))
     if rc != 0:
         raise ValueError(f"oracle expand rejected its arguments (rc={rc})")
     o["err"] = int(err[0])

@@ -45,6 +45,10 @@
 //     KV slot -1, hidden map -1 (h_shared), is_masked 0, rejected 1. new_token_idx =
 //     r*W + a_r + k; the scatter map sends target row r*(K+1)+j to drafter row r*W + j for
 //     j <= a_r and is -1 for the rejected target rows.
+//  R17 per-request draft counts in the rebuild (cu = exclusive prefix of K_r, as in the verify):
+//     L_r = a_r + K_r slots (K_r - 1 MASK slots), target hidden row of slot j = cu[r] + r + j,
+//     is_rejected[r][j] = 1 for 1 <= j <= K_r with j > a_r (0 past K_r), new_token_idx[r][k] =
+//     start_r + a_r + k for k < K_r and -1 after; a_r outside [0, K_r] is clamped.
 //
 // Build: g++ -std=c++17 -O2 -ffp-contract=off -fno-fast-math (no FMA contraction, so every
 // fp32 operation below is one IEEE-754 round-to-nearest operation on both x86-64 and aarch64).
@@ -65,6 +69,7 @@ constexpr int32_t ERR_NUM_ACCEPTED = 4;   // num_accepted outside [0, K]
 constexpr int32_t ERR_MAP_RANGE = 8;      // hidden map row outside the target hidden rows
 constexpr int32_t ERR_ZERO_ROW = 16;      // race row without a positive key even on p
 constexpr int32_t ERR_TOTAL_RANGE = 32;   // total_out outside [0, capacity]
+constexpr int32_t ERR_DRAFT_COUNT = 128;  // a per-request draft count outside [0, K]
 
 // ---------------------------------------------------------------- [PX] Philox4x32-10
 // One round: two 32x32->64 products, the high halves xor-ed with the other two words and the
@@ -460,17 +465,28 @@ int oracle_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t*
                          int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
                          int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
                          uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
-                         int32_t* new_token_idx, int32_t* total_out, int32_t* err) {
+                         int32_t* new_token_idx, int32_t* total_out, int32_t* err,
+                         const int32_t* cu) {
   if (B < 0 || K < 1 || block_size < 1 || max_blocks < 0) return -1;
   int32_t e = 0;
   long total = 0;
   for (int r = 0; r < B; ++r) {
-    int a = num_accepted[r];
-    if (a < 0 || a > K) {
-      e |= ERR_NUM_ACCEPTED;
-      a = std::min(std::max(a, 0), K);
+    int Kr = K;          // this request's draft count (R17)
+    long t0 = (long)r * (K + 1);  // its first target hidden row
+    if (cu) {
+      Kr = cu[r + 1] - cu[r];
+      if (Kr < 0 || Kr > K) {
+        e |= ERR_DRAFT_COUNT;
+        Kr = Kr < 0 ? 0 : K;
+      }
+      t0 = (long)cu[r] + r;
     }
-    const int L = a + K;
+    int a = num_accepted[r];
+    if (a < 0 || a > Kr) {
+      e |= ERR_NUM_ACCEPTED;
+      a = std::min(std::max(a, 0), Kr);
+    }
+    const int L = a + Kr;
     start_loc[r] = (int32_t)total;
     for (int j = 0; j < L; ++j) {
       const long i = total + j;
@@ -492,11 +508,13 @@ int oracle_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t*
         else slot = (int32_t)s;
       }
       slot_mapping[i] = slot;
-      hidden_map[i] = (j <= a) ? (int32_t)((long)r * (K + 1) + j) : -1;
+      hidden_map[i] = (j <= a) ? (int32_t)(t0 + j) : -1;
       is_masked[i] = (j > a) ? 1 : 0;
     }
-    for (int j = 0; j <= K; ++j) is_rejected[(long)r * (K + 1) + j] = (j >= 1 && j > a) ? 1 : 0;
-    for (int k = 0; k < K; ++k) new_token_idx[(long)r * K + k] = (int32_t)(total + a + k);
+    for (int j = 0; j <= K; ++j)
+      is_rejected[(long)r * (K + 1) + j] = (j >= 1 && j > a && j <= Kr) ? 1 : 0;
+    for (int k = 0; k < K; ++k)
+      new_token_idx[(long)r * K + k] = k < Kr ? (int32_t)(total + a + k) : -1;
     total += L;
   }
   start_loc[B] = (int32_t)total;

@@ -62,3 +62,42 @@ def test_zero_drafts_sample_the_bonus_from_p0():
         x, _ = oracle.race_row(p0[r], None, seed=44, r=r, j=0)
         assert rag["out_tokens"][r, 0] == x and rag["num_accepted"][r] == 0
         assert list(rag["out_tokens"][r, 1:]) == [-1, -1]
+
+
+def test_rebuild_with_per_request_counts_hand_example():
+    import json
+
+    from conftest import golden_path
+
+    g = json.load(open(golden_path("expand_ragged_hand_example.json")))
+    o = oracle.pdraft_expand(np.array(g["out_tokens"]), np.array(g["num_accepted"]),
+                             np.array(g["pos0"]), np.array(g["block_table"]), g["block_size"],
+                             g["mask_token_id"], cu=np.array(g["cu_drafts"]))
+    for k, v in g["expected"].items():
+        assert np.array_equal(np.ravel(o[k]), np.ravel(v)), k
+    assert o["err"] == 0
+
+
+def test_rebuild_uniform_counts_reproduce_the_batch_layout():
+    rng = np.random.default_rng(12)
+    B, K, bs = 20, 4, 16
+    a = rng.integers(0, K + 1, B).astype(np.int32)
+    toks = rng.integers(0, 500, (B, K + 1)).astype(np.int32)
+    pos0 = rng.integers(0, 300, B).astype(np.int32)
+    width = (int(pos0.max()) + 2 * K) // bs + 1
+    table = rng.permutation(B * width).astype(np.int32).reshape(B, width)
+    full = oracle.pdraft_expand(toks, a, pos0, table, bs, 500)
+    rag = oracle.pdraft_expand(toks, a, pos0, table, bs, 500,
+                               cu=np.arange(B + 1, dtype=np.int32) * K)
+    for k in ("input_ids", "positions", "slot_mapping", "hidden_map", "is_masked",
+              "is_rejected", "start_loc", "new_token_idx", "total_out"):
+        assert np.array_equal(full[k], rag[k]), k
+
+
+def test_rebuild_count_out_of_range_is_clamped_and_flagged():
+    toks = np.array([[5, 6, 7], [8, 9, 10]], np.int32)
+    o = oracle.pdraft_expand(toks, np.array([1, 0], np.int32), np.array([0, 0], np.int32),
+                             np.array([[0, 1], [2, 3]], np.int32), 16, 99,
+                             cu=np.array([0, 5, 5], np.int32))  # request 0 claims 5 > K = 2
+    assert o["err"] & oracle.ERR_DRAFT_COUNT
+    assert int(o["total_out"][0]) == (1 + 2) + (0 + 0)
