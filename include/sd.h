@@ -263,6 +263,29 @@ SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int3
                              void* stream);
 
 /*
+ * sd_pdraft_prepare_ragged -- sd_pdraft_prepare with a draft count per request, the rebuild
+ * that follows sd_verify_ragged (adaptive per-request k): request r with K_r = cu_drafts[r+1] -
+ * cu_drafts[r] drafts (0 <= K_r <= K_max) gets L_r = a_r + K_r drafter slots (its accepted
+ * drafts, its final token, K_r - 1 MASK slots); its target hidden rows are cu_drafts[r] + r ..
+ * (the packing sd_verify_ragged reads). is_rejected [B, K_max+1] is 1 for 1 <= j <= K_r with
+ * j > a_r; new_token_idx [B, K_max] is start_loc[r] + a_r + k for k < K_r and -1 after;
+ * num_accepted outside [0, K_r] is clamped (SD_ERR_NUM_ACCEPTED), a count outside [0, K_max]
+ * too (SD_ERR_DRAFT_COUNT). capacity B*2*K_max holds every outcome. Other arguments and outputs
+ * as for sd_pdraft_prepare (with K = K_max).
+ */
+SD_API int sd_pdraft_prepare_ragged(int B, int K_max, const int32_t* out_tokens,
+                                    const int32_t* num_accepted, const int32_t* cu_drafts,
+                                    const int32_t* pos0, const int32_t* block_table,
+                                    int max_blocks, int block_size, int32_t mask_token_id,
+                                    int capacity, int32_t* input_ids, int32_t* positions,
+                                    int32_t* slot_mapping, int32_t* hidden_map,
+                                    uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
+                                    int32_t* new_token_idx, int32_t* total_out, int H,
+                                    const void* target_hidden, long ld_in, int n_in_rows,
+                                    const void* h_shared, void* out_hidden, long ld_out,
+                                    int32_t* err, void* stream);
+
+/*
  * sd_pdraft_prepare_padded -- the drafter batch in fixed-width rows, with its hidden states.
  *
  * P-EAGLE blog (vLLM), sections "并行草稿生成的挑战" and "Triton Kernel" (the rebuilt ids,

@@ -68,6 +68,9 @@ def test_host_argument_checks(lib):
     assert lib.sd_draft_sample(2, 3, 10, 0, 16, 10, P, 0, 2**32 - 1, 16, P, P) == -2
     assert lib.sd_draft_sample(2, 3, 10, 0, P, 10, P, 0, 0, 16, P, P) == -1
     assert lib.sd_draft_sample(0, 3, 10, 0, P, 10, P, 0, 0, P, P, P) == 0
+    # ragged rebuild: the prefix of counts is required
+    assert lib.sd_pdraft_prepare_ragged(1, 2, 16, 16, P, 16, 16, 1, 16, 0, 4, *([16] * 9), 8,
+                                        16, 8, 1, 16, 16, 8, P, P) == -1
     # padded rebuild: K range, null outputs, empty batch
     assert lib.sd_pdraft_prepare_padded(1, 0, *([P] * 4), 1, 16, 0, *([P] * 8), 8, P, 8, 0, P, P,
                                         8, P, P) == -2

@@ -32,7 +32,7 @@ SD_ERR_DRAFT_COUNT = 128
 
 EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
             "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_prepare_padded",
-            "sd_verify_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
+            "sd_verify_ragged", "sd_pdraft_prepare_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
@@ -76,6 +76,10 @@ def load():
                                           P, P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P, i64,
                                           P, P]
         lib.sd_pdraft_prepare.restype = i32
+        lib.sd_pdraft_prepare_ragged.argtypes = [i32, i32, P, P, P, P, P, i32, i32,
+                                                 ctypes.c_int32, i32, P, P, P, P, P, P, P, P, P,
+                                                 i32, P, i64, i32, P, P, i64, P, P]
+        lib.sd_pdraft_prepare_ragged.restype = i32
         lib.sd_pdraft_prepare_padded.argtypes = [i32, i32, P, P, P, P, i32, i32, ctypes.c_int32,
                                                  P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P,
                                                  i64, P, P]
@@ -270,6 +274,25 @@ def sd_pdraft_prepare(out_tokens, num_accepted, pos0, block_table, block_size, m
         _row_stride(target_hidden), target_hidden.shape[0], _ptr(h_shared), _ptr(out_hidden),
         _row_stride(out_hidden), _ptr(err), _stream(start_loc, stream))
     _check(rc, "sd_pdraft_prepare")
+
+
+def sd_pdraft_prepare_ragged(out_tokens, num_accepted, cu_drafts, pos0, block_table, block_size,
+                             mask_token_id, input_ids, positions, slot_mapping, hidden_map,
+                             is_masked, is_rejected, start_loc, new_token_idx, total_out,
+                             target_hidden, h_shared, out_hidden, err=None, stream=None):
+    """sd_pdraft_prepare with a draft count per request (see include/sd.h)."""
+    B, K1 = out_tokens.shape
+    cap, H = out_hidden.shape
+    if input_ids.shape[0] != cap or cu_drafts.shape[0] != B + 1:
+        raise SDError("out_hidden needs one row per drafter slot, cu_drafts B+1 entries")
+    rc = load().sd_pdraft_prepare_ragged(
+        B, K1 - 1, _ptr(out_tokens), _ptr(num_accepted), _ptr(cu_drafts), _ptr(pos0),
+        _ptr(block_table), block_table.shape[1], block_size, mask_token_id, cap, _ptr(input_ids),
+        _ptr(positions), _ptr(slot_mapping), _ptr(hidden_map), _ptr(is_masked),
+        _ptr(is_rejected), _ptr(start_loc), _ptr(new_token_idx), _ptr(total_out), H,
+        _ptr(target_hidden), _row_stride(target_hidden), target_hidden.shape[0], _ptr(h_shared),
+        _ptr(out_hidden), _row_stride(out_hidden), _ptr(err), _stream(start_loc, stream))
+    _check(rc, "sd_pdraft_prepare_ragged")
 
 
 def sd_pdraft_prepare_padded(out_tokens, num_accepted, pos0, block_table, block_size,

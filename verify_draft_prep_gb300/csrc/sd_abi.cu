@@ -17,10 +17,10 @@ int sd_verify_noalloc_launch(int, int, int, int, const void*, long, const void*,
 int sd_verify_kernel_count(int, int, int, int);
 int sd_sample_launch(int, int, int, int, const void*, long, const float*, uint64_t, uint32_t,
                      int32_t*, int32_t*, cudaStream_t);
-int sd_prep_launch(int, int, const int32_t*, const int32_t*, const int32_t*, const int32_t*, int,
-                   int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
-                   int32_t*, int32_t*, int32_t*, int, const void*, long, int, const void*, void*,
-                   long, int32_t*, cudaStream_t);
+int sd_prep_launch(int, int, const int32_t*, const int32_t*, const int32_t*, const int32_t*,
+                   const int32_t*, int, int, int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*,
+                   uint8_t*, uint8_t*, int32_t*, int32_t*, int32_t*, int, const void*, long, int,
+                   const void*, void*, long, int32_t*, cudaStream_t);
 int sd_prep_padded_launch(int, int, const int32_t*, const int32_t*, const int32_t*,
                           const int32_t*, int, int, int32_t, int32_t*, int32_t*, int32_t*,
                           int32_t*, uint8_t*, uint8_t*, int32_t*, int32_t*, int, const void*, long,
@@ -207,20 +207,20 @@ int sd_pdraft_expand(int B, int K, const int32_t* out_tokens, const int32_t* num
   if (rc != SD_OK) return rc;
   rc = check_device();
   if (rc != SD_OK) return rc;
-  return sd_prep_launch(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks, block_size,
-                        mask_token_id, capacity, input_ids, positions, slot_mapping, hidden_map,
-                        is_masked, is_rejected, start_loc, new_token_idx, total_out, 0, nullptr,
-                        0, 0, nullptr, nullptr, 0, err, (cudaStream_t)stream);
+  return sd_prep_launch(B, K, out_tokens, num_accepted, nullptr, pos0, block_table, max_blocks,
+                        block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
+                        hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out,
+                        0, nullptr, 0, 0, nullptr, nullptr, 0, err, (cudaStream_t)stream);
 }
 
-int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
-                      const int32_t* pos0, const int32_t* block_table, int max_blocks,
-                      int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
-                      int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
-                      uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
-                      int32_t* new_token_idx, int32_t* total_out, int H,
-                      const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared,
-                      void* out_hidden, long ld_out, int32_t* err, void* stream) {
+namespace {
+int prepare(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
+            const int32_t* cu_drafts, const int32_t* pos0, const int32_t* block_table,
+            int max_blocks, int block_size, int32_t mask_token_id, int capacity,
+            int32_t* input_ids, int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
+            uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc, int32_t* new_token_idx,
+            int32_t* total_out, int H, const void* target_hidden, long ld_in, int n_in_rows,
+            const void* h_shared, void* out_hidden, long ld_out, int32_t* err, void* stream) {
   int rc = check_expand_args(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks,
                              block_size, capacity, input_ids, positions, slot_mapping, hidden_map,
                              is_masked, is_rejected, start_loc, new_token_idx, total_out);
@@ -233,11 +233,43 @@ int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int32_t* nu
   rc = check_device();
   if (rc != SD_OK) return rc;
   if (capacity == 0) out_hidden = nullptr;
-  return sd_prep_launch(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks, block_size,
-                        mask_token_id, capacity, input_ids, positions, slot_mapping, hidden_map,
-                        is_masked, is_rejected, start_loc, new_token_idx, total_out, H,
-                        target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
-                        (cudaStream_t)stream);
+  return sd_prep_launch(B, K, out_tokens, num_accepted, cu_drafts, pos0, block_table,
+                        max_blocks, block_size, mask_token_id, capacity, input_ids, positions,
+                        slot_mapping, hidden_map, is_masked, is_rejected, start_loc,
+                        new_token_idx, total_out, H, target_hidden, ld_in, n_in_rows, h_shared,
+                        out_hidden, ld_out, err, (cudaStream_t)stream);
+}
+}  // namespace
+
+int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
+                      const int32_t* pos0, const int32_t* block_table, int max_blocks,
+                      int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
+                      int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
+                      uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
+                      int32_t* new_token_idx, int32_t* total_out, int H,
+                      const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared,
+                      void* out_hidden, long ld_out, int32_t* err, void* stream) {
+  return prepare(B, K, out_tokens, num_accepted, nullptr, pos0, block_table, max_blocks,
+                 block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
+                 hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out, H,
+                 target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err, stream);
+}
+
+int sd_pdraft_prepare_ragged(int B, int K_max, const int32_t* out_tokens,
+                             const int32_t* num_accepted, const int32_t* cu_drafts,
+                             const int32_t* pos0, const int32_t* block_table, int max_blocks,
+                             int block_size, int32_t mask_token_id, int capacity,
+                             int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
+                             int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
+                             int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out,
+                             int H, const void* target_hidden, long ld_in, int n_in_rows,
+                             const void* h_shared, void* out_hidden, long ld_out, int32_t* err,
+                             void* stream) {
+  if (B > 0 && !cu_drafts) return SD_E_NULL;
+  return prepare(B, K_max, out_tokens, num_accepted, cu_drafts, pos0, block_table, max_blocks,
+                 block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
+                 hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out, H,
+                 target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err, stream);
 }
 
 int sd_pdraft_prepare_padded(int B, int K, const int32_t* out_tokens,

@@ -31,6 +31,7 @@ struct PrepParams {
   int B, K;
   const int32_t* out_tokens;
   const int32_t* num_accepted;
+  const int32_t* cu;  // nullable: per-request draft counts as a prefix [B+1] (K is then K_max)
   const int32_t* pos0;
   const int32_t* block_table;
   int max_blocks, block_size;
@@ -86,11 +87,31 @@ __device__ __forceinline__ int clamp_acc(int a, int K, int32_t& e) {
   return a;
 }
 
+// Request r's draft count K_r (cu[r+1] - cu[r], clamped to [0, K] with SD_ERR_DRAFT_COUNT; K
+// without cu) and the index c0 with its first target hidden row at c0 + r.
+__device__ __forceinline__ int draft_count(const int32_t* cu, int r, int K, int& c0,
+                                           int32_t& e) {
+  if (!cu) {
+    c0 = r * K;
+    return K;
+  }
+  c0 = __ldg(cu + r);
+  int k = __ldg(cu + r + 1) - c0;
+  if (k < 0 || k > K || c0 < 0) {
+    e |= SD_ERR_DRAFT_COUNT;
+    k = (k < 0 || c0 < 0) ? 0 : K;
+    c0 = c0 < 0 ? 0 : c0;
+  }
+  return k;
+}
+
 template <bool GATHER>
 __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   __shared__ int s_off[RPC_MAX + 1];  // local exclusive offsets of the CTA's requests
   __shared__ int s_a[RPC_MAX];
   __shared__ int s_pos[RPC_MAX];
+  __shared__ int s_k[RPC_MAX];   // draft counts
+  __shared__ int s_c0[RPC_MAX];  // first target hidden row - r
   __shared__ long long s_red[2][PNT / 32];
   __shared__ int s_wtot[PNT / 32];
   __shared__ int s_err;
@@ -115,7 +136,9 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   long long pre = 0, tot = 0;
   for (int r = tid; r < P.B; r += PNT) {
     int32_t ignored = 0;
-    const long long L = clamp_acc(P.num_accepted[r], K, ignored) + K;
+    int c0;
+    const int kr = draft_count(P.cu, r, K, c0, ignored);
+    const long long L = clamp_acc(P.num_accepted[r], kr, ignored) + kr;
     tot += L;
     pre += (r < r0) ? L : 0;
   }
@@ -141,10 +164,11 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   int running = 0;
   for (int c = 0; c < nreq; c += PNT) {
     const int q = c + tid;
-    int a = 0, L = 0;
+    int a = 0, L = 0, kr = 0, c0 = 0;
     if (q < nreq) {
-      a = clamp_acc(c == 0 ? a_first : P.num_accepted[r0 + q], K, e);
-      L = a + K;
+      kr = draft_count(P.cu, r0 + q, K, c0, e);
+      a = clamp_acc(c == 0 ? a_first : P.num_accepted[r0 + q], kr, e);
+      L = a + kr;
     }
     int incl = L;
 #pragma unroll
@@ -164,6 +188,8 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
     if (q < nreq) {
       s_off[q] = running + woff + incl - L;
       s_a[q] = a;
+      s_k[q] = kr;
+      s_c0[q] = c0;
     }
     running += ctot;
   }
@@ -175,11 +201,12 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   for (int q = tid; q < nreq; q += PNT) P.start_loc[r0 + q] = (int32_t)(pre + s_off[q]);
   for (int i = tid; i < nreq * K; i += PNT) {
     const int q = i / K, k = i - q * K;
-    P.new_token_idx[(size_t)r0 * K + i] = (int32_t)(pre + s_off[q] + s_a[q] + k);
+    P.new_token_idx[(size_t)r0 * K + i] =
+        k < s_k[q] ? (int32_t)(pre + s_off[q] + s_a[q] + k) : -1;
   }
   for (int i = tid; i < nreq * (K + 1); i += PNT) {
     const int q = i / (K + 1), j = i - q * (K + 1);
-    P.is_rejected[(size_t)r0 * (K + 1) + i] = (j >= 1 && j > s_a[q]) ? 1 : 0;
+    P.is_rejected[(size_t)r0 * (K + 1) + i] = (j >= 1 && j > s_a[q] && j <= s_k[q]) ? 1 : 0;
   }
 
   // this CTA's drafter slots
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
     P.input_ids[g] = tok;
     P.positions[g] = (int32_t)pos;
     P.slot_mapping[g] = slot;
-    P.hidden_map[g] = (j <= a) ? (int32_t)((long long)rq * (K + 1) + j) : -1;
+    P.hidden_map[g] = (j <= a) ? (int32_t)((long long)s_c0[q] + rq + j) : -1;
     P.is_masked[g] = (j > a) ? 1 : 0;
   }
 
@@ -232,7 +259,8 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
   }
 
   if (GATHER) {
-    // one warp per drafter row: target hidden row r*(K+1)+j for j <= a_r, h_shared otherwise
+    // one warp per drafter row: target hidden row r*(K+1)+j (cu[r]+r+j with per-request counts)
+    // for j <= a_r, h_shared otherwise
     const long long nrows = min((long long)local_total, (long long)P.capacity - pre);
     for (long long i = warp; i < nrows; i += PNT / 32) {
       int lo = 0, hi = nreq - 1;
@@ -242,7 +270,7 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
         else hi = mid - 1;
       }
       const int q = lo, j = (int)i - s_off[q];
-      const long long m = (j <= s_a[q]) ? (long long)(r0 + q) * (K + 1) + j : -1;
+      const long long m = (j <= s_a[q]) ? (long long)s_c0[q] + (r0 + q) + j : -1;
       const uint16_t* src = P.h_shared;
       if (m >= 0) {
         if (m < P.n_in_rows) src = P.hidden + m * P.ld_in;
@@ -366,7 +394,7 @@ __global__ void __launch_bounds__(PNT) prep_padded_kernel(const PaddedParams P) 
 }  // namespace sdk
 
 extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
-                              const int32_t* pos0, const int32_t* block_table, int max_blocks,
+                              const int32_t* cu_drafts, const int32_t* pos0, const int32_t* block_table, int max_blocks,
                               int block_size, int32_t mask_token_id, int capacity,
                               int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
                               int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
@@ -379,6 +407,7 @@ extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int
   P.K = K;
   P.out_tokens = out_tokens;
   P.num_accepted = num_accepted;
+  P.cu = cu_drafts;
   P.pos0 = pos0;
   P.block_table = block_table;
   P.max_blocks = max_blocks;
