@@ -591,16 +591,50 @@ def run_e2e(sd, w, device, steps):
         e.record(stream)
         stream.synchronize()
     ms = s.elapsed_time(e) / steps
+
+    # The same calls given the pinned host arrays themselves: the kernels read over the host link
+    # only what the step needs (the rows up to the first rejection, the accepted hidden rows)
+    wz = W()
+    for k, v in vars(w).items():
+        setattr(wz, k, v)
+    for k, v in host.items():
+        setattr(wz, k, v)
+    if getattr(w, "_temp_arg", None) is not None:
+        wz._temp_arg = host["temperature"]
+
+    def step_zero_copy():
+        launch_step(sd, wz, o, stream)
+        for k in res_keys:
+            back[k].copy_(o[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step_zero_copy()
+        stream.synchronize()
+        sz, ez = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sz.record(stream)
+        for _ in range(steps):
+            step_zero_copy()
+        ez.record(stream)
+        stream.synchronize()
+    ms_zc = sz.elapsed_time(ez) / steps
+    a = o["num_accepted"].cpu().numpy()
+    rows_read = algorithmic_bytes(w, a)[3] + int(((a.astype(np.int64) + 1) * 2 * w.H).sum())
     world = 1
     import torch.distributed as dist
 
     if dist.is_initialized():  # the job's rate: every rank's requests over the slowest rank
         world = dist.get_world_size()
-        t = torch.tensor([ms], device=device)
+        t = torch.tensor([ms, ms_zc], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms, ms_zc = float(t[0].item()), float(t[1].item())
     return {"value": world * w.B / (ms * 1e-3), "unit": "requests/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "zero_copy": {"value": world * w.B / (ms_zc * 1e-3), "unit": "requests/s",
+                          "ms_per_step": ms_zc, "host_bytes_read_per_step": rows_read,
+                          "d2h_bytes_per_step": d2h,
+                          "how": "the same public calls given the pinned host input arrays; the "
+                                 "kernels read over the host link only the rows the step needs"}}
 
 
 def run_reference(args, world):

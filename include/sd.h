@@ -9,8 +9,11 @@
  *   sd_hidden_gather  drafter hidden states from the target's hidden states or h_shared.
  *
  * Conventions for every call:
- *   - Every pointer is a DEVICE pointer owned by the caller. The library allocates nothing and
- *     keeps no state between calls.
+ *   - Every pointer is a DEVICE pointer owned by the caller, or, for the read-only row inputs
+ *     (target, draft, hidden states), host memory the GPU can address (page-locked or
+ *     registered): the kernels then read over the host link only the parts the step needs.
+ *     Outputs, the workspace and *err are device memory. The library allocates nothing and keeps
+ *     no state between calls.
  *   - Calls only enqueue work on `stream` (a cudaStream_t; 0 = the legacy default stream) and
  *     never synchronise, so a step can be captured in a CUDA graph.
  *   - The return value is SD_OK or a negative SD_E_* code for errors the host can see (null

@@ -214,3 +214,21 @@ def test_request_base_shards_reproduce_the_whole_batch(temperature):
     if temperature is None:
         shifted = run_verify(pt[s * (K + 1):], qt[s * K:], dt[s:], None, seed=7)
         assert not np.array_equal(shifted["out_tokens"], hi["out_tokens"])
+
+
+def test_pinned_host_inputs_match_device_inputs():
+    # the kernels may read their row inputs straight from pinned host memory (over the host link)
+    rng = np.random.default_rng(61)
+    B, K, V = 6, 3, 20011
+    p, q, d, T = random_probs_case(rng, B, K, V, greedy_frac=0.3)
+    dev = run_verify(to_dev(p), to_dev(q), to_dev(d), to_dev(T), seed=5)
+    hp = torch.from_numpy(p).pin_memory()
+    hq = torch.from_numpy(q).pin_memory()
+    out = dict(out_tokens=torch.empty(B, K + 1, dtype=torch.int32, device="cuda"),
+               num_accepted=torch.empty(B, dtype=torch.int32, device="cuda"))
+    sd.sd_verify(hp, hq, to_dev(d), out["out_tokens"], out["num_accepted"],
+                 temperature=to_dev(T), seed=5,
+                 workspace_buf=torch.zeros(16 * B, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert np.array_equal(out["out_tokens"].cpu().numpy(), dev["out_tokens"])
+    assert np.array_equal(out["num_accepted"].cpu().numpy(), dev["num_accepted"])

@@ -107,11 +107,20 @@ def _check(rc: int, what: str):
 
 
 def _ptr(t):
+    """Device pointer of a tensor on the GPU, or of a pinned host tensor (page-locked host memory
+    is addressable by the GPU: the kernels then read it over the host link)."""
     if t is None:
         return None
-    if not t.is_cuda:
-        raise SDError("tensors passed to libsd_gb300 must live on the GPU")
+    if not (t.is_cuda or t.is_pinned()):
+        raise SDError("tensors passed to libsd_gb300 must live on the GPU or in pinned memory")
     return t.data_ptr()
+
+
+def _device(t):
+    """The tensor's GPU, or the current GPU for a pinned host tensor."""
+    import torch
+
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
 
 
 def _stream(t, stream):
@@ -119,7 +128,8 @@ def _stream(t, stream):
 
     if stream is not None:
         return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    return torch.cuda.current_stream(t.device).cuda_stream
+    # a pinned host tensor has no device of its own: the current device's stream
+    return torch.cuda.current_stream(_device(t)).cuda_stream
 
 
 def _row_stride(t):
@@ -171,7 +181,8 @@ def sd_verify(target, draft, drafts, out_tokens, num_accepted, temperature=None,
         raise SDError("draft must match target's dtype and vocabulary")
     if target.shape[0] != B * (K + 1) or draft.shape[0] != B * K:
         raise SDError("row counts must be B*(K+1) (target) and B*K (draft)")
-    ws = workspace_buf if workspace_buf is not None else workspace(target.device, B, K, V, dtype)
+    ws = workspace_buf if workspace_buf is not None else workspace(_device(target), B, K, V,
+                                                                   dtype)
     rc = load().sd_verify(B, K, V, dtype, _ptr(target), _row_stride(target), _ptr(draft),
                           _row_stride(draft), _ptr(drafts), _ptr(temperature), seed,
                           request_base, _ptr(out_tokens), _ptr(num_accepted), _ptr(p_at_draft),
@@ -200,7 +211,7 @@ def sd_verify_ragged(target, draft, drafts, cu_drafts, out_tokens, num_accepted,
         raise SDError("target must be float32 probabilities or bfloat16 logits")
     if draft.dtype != target.dtype or cu_drafts.shape[0] != B + 1:
         raise SDError("draft must match target; cu_drafts needs B+1 entries")
-    ws = workspace_buf if workspace_buf is not None else workspace(target.device, B, K1 - 1, V,
+    ws = workspace_buf if workspace_buf is not None else workspace(_device(target), B, K1 - 1, V,
                                                                    dtype)
     rc = load().sd_verify_ragged(B, K1 - 1, V, dtype, _ptr(target), _row_stride(target),
                                  _ptr(draft), _row_stride(draft) if draft.shape[0] else V,
