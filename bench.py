@@ -38,10 +38,10 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "a10a92db30eb38db"): (82.316288e6, "ncu --set full, one launch of the full batch"),
-    ("b256mix", "a10a92db30eb38db"): (439.077376e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "a10a92db30eb38db"): (783.758944e6, "ncu --set full at B=160, scaled x3.2"),
-    ("b1024lg", "a10a92db30eb38db"): (3025.6142e6, "ncu --set full at B=96, scaled x1024/96"),
+    ("b64", "b4e06989d953523a"): (82.746368e6, "ncu --set full, one launch of the full batch"),
+    ("b256mix", "b4e06989d953523a"): (439.775744e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "b4e06989d953523a"): (783.75895e6, "ncu --set full at B=160, scaled x3.2"),
+    ("b1024lg", "b4e06989d953523a"): (3023.7027e6, "ncu --set full at B=96, scaled x1024/96"),
 }
 
 
