@@ -340,13 +340,21 @@ SD_API int sd_hidden_gather(int capacity, int H, const int32_t* total_out, const
 /* Philox4x32-10 of n counters ctr[n][4] under key (seed lo, seed hi) -> out[n][4]. */
 SD_API int sd_philox_words(int n, const uint32_t* ctr, uint64_t seed, uint32_t* out, void* stream);
 
-/* The race variates E = fp32(-log((w + 0.5) * 2^-32)) of n words w[n] -> E[n] (the exact path). */
+/* The race variates E = fp32(-log((w + 0.5) * 2^-32)) of n words w[n] -> E[n] (the exact path
+ * the kernels use). */
 SD_API int sd_race_E(int n, const uint32_t* w, float* E, void* stream);
 
 /* Worst relative error, over every w in [w_begin, w_begin + count), of the fast approximation
  * the race filter uses for -log(v) against the exact E above. Writes max_rel[0] (fp32,
  * caller-zeroed) with atomicMax on the float bits. */
 SD_API int sd_race_E_approx_error(uint32_t w_begin, uint64_t count, float* max_rel, void* stream);
+
+/* Bit-exactness check of the exact race variate: the kernels evaluate E from pairs of fp32 and
+ * take the double path only near an fp32 rounding boundary. Over every w in
+ * [w_begin, w_begin + count) adds to counts[0] (uint64, caller-zeroed) the words whose E differs
+ * from the double path's fp32(-log((w + 0.5) * 2^-32)), and to counts[1] the words that took
+ * the double path. */
+SD_API int sd_race_E_check(uint32_t w_begin, uint64_t count, uint64_t* counts, void* stream);
 
 /* Text for a status code (static storage). */
 SD_API const char* sd_status_string(int status);

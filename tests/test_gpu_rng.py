@@ -60,3 +60,16 @@ def test_race_filter_approximation_bound_exhaustive():
     worst = out.item()
     print(f"worst relative error of the race filter's 1/E approximation: {worst:.3e}")
     assert 0 < worst <= 2.0**-10
+
+
+def test_pair_evaluated_E_is_the_double_path_on_every_word():
+    # The kernels form E from pairs of fp32 and take the double log only where the pair's value
+    # lies within 2^-36 of an fp32 rounding boundary; over all 2^32 words that must give the
+    # double path's value bit for bit, with the double path taken rarely (about 1 word in 2900).
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    sd.sd_race_E_check(0, 1 << 32, counts)
+    torch.cuda.synchronize()
+    mismatches, near = (int(v) for v in counts.cpu())
+    print(f"pair-evaluated E: {mismatches} mismatches, {near} words on the double path")
+    assert mismatches == 0
+    assert 0 < near < (1 << 32) // 1000

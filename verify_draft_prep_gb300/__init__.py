@@ -33,7 +33,7 @@ SD_ERR_DRAFT_COUNT = 128
 EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
             "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_prepare_padded",
             "sd_verify_ragged", "sd_pdraft_prepare_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
-            "sd_race_E_approx_error", "sd_status_string", "sd_version"]
+            "sd_race_E_approx_error", "sd_race_E_check", "sd_status_string", "sd_version"]
 
 _lock = threading.Lock()
 _lib = None
@@ -92,6 +92,8 @@ def load():
         lib.sd_race_E.restype = i32
         lib.sd_race_E_approx_error.argtypes = [u32, u64, P, P]
         lib.sd_race_E_approx_error.restype = i32
+        lib.sd_race_E_check.argtypes = [u32, u64, P, P]
+        lib.sd_race_E_check.restype = i32
         lib.sd_status_string.argtypes = [i32]
         lib.sd_status_string.restype = ctypes.c_char_p
         lib.sd_version.argtypes = []
@@ -353,3 +355,10 @@ def sd_race_E(w, E, stream=None):
 def sd_race_E_approx_error(w_begin, count, max_rel, stream=None):
     rc = load().sd_race_E_approx_error(w_begin, count, _ptr(max_rel), _stream(max_rel, stream))
     _check(rc, "sd_race_E_approx_error")
+
+
+def sd_race_E_check(w_begin, count, counts, stream=None):
+    """counts: int64 CUDA tensor [2], zeroed: (words differing from the double path, words that
+    took the double path) over [w_begin, w_begin + count)."""
+    rc = load().sd_race_E_check(w_begin, count, _ptr(counts), _stream(counts, stream))
+    _check(rc, "sd_race_E_check")

@@ -30,6 +30,7 @@ int sd_gather_launch(int, int, const int32_t*, const int32_t*, const void*, long
 int sd_philox_launch(int, const uint32_t*, uint64_t, uint32_t*, cudaStream_t);
 int sd_race_E_launch(int, const uint32_t*, float*, cudaStream_t);
 int sd_approx_error_launch(uint32_t, uint64_t, float*, cudaStream_t);
+int sd_E_check_launch(uint32_t, uint64_t, unsigned long long*, cudaStream_t);
 }
 
 namespace {
@@ -340,6 +341,15 @@ int sd_race_E_approx_error(uint32_t w_begin, uint64_t count, float* max_rel, voi
   const int dev = check_device();
   if (dev != SD_OK) return dev;
   return sd_approx_error_launch(w_begin, count, max_rel, (cudaStream_t)stream);
+}
+
+int sd_race_E_check(uint32_t w_begin, uint64_t count, uint64_t* counts, void* stream) {
+  if (count > (1ull << 32)) return SD_E_SHAPE;
+  if (!counts) return SD_E_NULL;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_E_check_launch(w_begin, count, reinterpret_cast<unsigned long long*>(counts),
+                           (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -100,9 +100,113 @@ __device__ __forceinline__ double accept_uniform(const PhiloxRoundKeys& rk, uint
 }
 
 // Exact race variate: E = fp32 rounding of the double -log(v), v = (w + 0.5) * 2^-32 (exact).
-__device__ __forceinline__ float race_E_exact(uint32_t w) {
+__device__ __forceinline__ float race_E_exact_double(uint32_t w) {
   const double v = ((double)w + 0.5) * (1.0 / 4294967296.0);
   return __double2float_rn(-log(v));
+}
+
+// ---------------------------------------------------------------------------------------------
+// The same E from pairs of fp32 (hi + lo, about 48 significant bits), because GB300 runs FP64 at a
+// small fraction of its FP32 rate (one double log costs a warp about 2000 cycles). -ln v is formed
+// from the series 2 atanh(z) = 2 (z + z^3/3 + z^5/5 + ...):
+//   v >= 1/sqrt(2): u = 1 - v (exact from the integer 2^32 - 1 - w), -ln v = 2 atanh(u / (2 - u));
+//   v <  1/sqrt(2): v = 2^(k-32) m with m in [1/sqrt(2), sqrt(2)), -ln v = (32 - k) ln 2 - ln m,
+//                   ln m = 2 atanh((m - 1) / (m + 1)).
+// |z| <= 0.1716 in both, so the series to z^17 leaves a relative truncation below 2^-49; the
+// pair arithmetic (error-free sums and FMA products) keeps the whole evaluation within about
+// 2^-44. The pair's hi is its fp32 rounding; where the value lies within 2^-36 (relative) of an
+// fp32 rounding boundary the double path decides instead, so the result is always the double
+// path's (checked against it on the GPU over all 2^32 words).
+// ---------------------------------------------------------------------------------------------
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return FF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {  // |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const FF s = ff_two_sum(a.hi, b.hi);
+  return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = fmaf(a.hi, b.hi, -p);  // the exact error of p
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return ff_fast_two_sum(p, e);
+}
+__device__ __forceinline__ FF ff_div(FF a, FF b) {
+  const float q1 = __fdiv_rn(a.hi, b.hi);
+  const FF p = ff_mul(FF{q1, 0.0f}, b);
+  const FF r = ff_add(a, FF{-p.hi, -p.lo});
+  return ff_fast_two_sum(q1, __fdiv_rn(r.hi, b.hi));
+}
+
+// 2 atanh(z) = 2z (1 + t/3 + t^2/5 + ... + t^8/17), t = z^2 <= 0.0295: the five leading
+// coefficients in pairs, the tail in fp32.
+__device__ __forceinline__ FF ff_two_atanh(FF z) {
+  const FF t = ff_mul(z, z);
+  const float tf = t.hi;
+  float q = fmaf(tf, 0x1.e1e1e2p-5f /*1/17*/, 0x1.111112p-4f /*1/15*/);
+  q = fmaf(tf, q, 0x1.3b13b2p-4f /*1/13*/);
+  q = fmaf(tf, q, 0x1.745d18p-4f /*1/11*/);
+  FF a = ff_add(FF{0x1.c71c72p-4f, -0x1.c71c72p-31f} /*1/9*/, ff_mul(t, FF{q, 0.0f}));
+  a = ff_add(FF{0x1.24924ap-3f, -0x1.b6db6ep-28f} /*1/7*/, ff_mul(t, a));
+  a = ff_add(FF{0x1.99999ap-3f, -0x1.99999ap-29f} /*1/5*/, ff_mul(t, a));
+  a = ff_add(FF{0x1.555556p-2f, -0x1.555556p-27f} /*1/3*/, ff_mul(t, a));
+  const FF P = ff_add(FF{1.0f, 0.0f}, ff_mul(t, a));
+  return ff_mul(FF{2.0f * z.hi, 2.0f * z.lo}, P);
+}
+
+// The fp32 rounding of the pair's value; near = true where it may lie within 2^-36 (relative) of
+// a rounding boundary, and the caller takes the double path.
+__device__ __forceinline__ float race_E_pair(uint32_t w, bool& near) {
+  FF y;
+  if (w >= 0xB504F334u) {  // v >= 1/sqrt(2)
+    const uint32_t n = 0xFFFFFFFFu - w;  // u = (n + 0.5) 2^-32 = 1 - v, n < 2^31
+    const FF u = ff_two_sum(__uint2float_rn(n & ~0xFFu) * 0x1p-32f,
+                            (__uint2float_rn(n & 0xFFu) + 0.5f) * 0x1p-32f);
+    const FF d = ff_add(FF{2.0f, 0.0f}, FF{-u.hi, -u.lo});
+    y = ff_two_atanh(ff_div(u, d));
+  } else {
+    FF x = ff_two_sum(__uint2float_rn(w & ~0xFFu), __uint2float_rn(w & 0xFFu) + 0.5f);
+    int k = (int)((__float_as_uint(x.hi) >> 23) & 0xFFu) - 127;  // x.hi in [2^k, 2^(k+1))
+    float sc = __uint_as_float((uint32_t)(127 - k) << 23);        // 2^-k, exact
+    FF m{x.hi * sc, x.lo * sc};
+    if (m.hi > 1.41421356f) {
+      ++k;
+      m.hi *= 0.5f;
+      m.lo *= 0.5f;
+    }
+    const FF lnm = ff_two_atanh(ff_div(ff_add(m, FF{-1.0f, 0.0f}), ff_add(m, FF{1.0f, 0.0f})));
+    const float K = (float)(32 - k);                          // 1..33
+    const float l2lo = __fmul_rn(K, 0x1.7f7d1cp-20f);         // K ln2, second part
+    FF kl = ff_fast_two_sum(__fmul_rn(K, 0x1.62e4p-1f),        // exact (17 x 6 bits)
+                            l2lo);
+    kl = ff_add(kl, FF{fmaf(K, 0x1.7f7d1cp-20f, -l2lo), __fmul_rn(K, 0x1.ef357ap-45f)});
+    y = ff_add(kl, FF{-lnm.hi, -lnm.lo});
+  }
+  // y.hi is the pair's fp32 rounding; accept it unless the value may lie near a boundary
+  const uint32_t hb = __float_as_uint(y.hi);
+  const float ulp = __uint_as_float(hb & 0x7F800000u) * 0x1p-23f;
+  const bool pow2 = (hb & 0x007FFFFFu) == 0u;
+  const float half = (y.lo < 0.0f && pow2) ? 0.25f * ulp : 0.5f * ulp;
+  near = !(fabsf(y.lo) + y.hi * 0x1p-36f < half);
+  return y.hi;
+}
+
+// Exact race variate: the pair's rounding, or the double path near a rounding boundary (about
+// one word in 2900); bit for bit the double path's value for every w.
+__device__ __forceinline__ float race_E_exact(uint32_t w) {
+  bool near;
+  const float e = race_E_pair(w, near);
+  return near ? race_E_exact_double(w) : e;
 }
 
 // Fast filter value for the race: R ~= 2^64 / (-log2 v), proportional to 1/E, from one hardware

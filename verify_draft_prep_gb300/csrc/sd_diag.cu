@@ -42,6 +42,32 @@ __global__ void approx_error_kernel(uint32_t w_begin, unsigned long long count, 
   }
 }
 
+// Counts, over every w in [w_begin, w_begin + count), the words where the exact race variate
+// differs from the double path (counts[0]) and the words that took the double path (counts[1]).
+__global__ void E_check_kernel(uint32_t w_begin, unsigned long long count,
+                               unsigned long long* counts) {
+  unsigned long long mis = 0, near_n = 0;
+  for (unsigned long long k = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+       k < count; k += (unsigned long long)gridDim.x * blockDim.x) {
+    const uint32_t w = (uint32_t)(w_begin + k);
+    bool near;
+    const float e = race_E_pair(w, near);
+    near_n += near;
+    const float got = near ? race_E_exact_double(w) : e;
+    // the reference value: the double path for every word
+    mis += __float_as_uint(got) != __float_as_uint(race_E_exact_double(w));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mis += __shfl_xor_sync(0xffffffffu, mis, o);
+    near_n += __shfl_xor_sync(0xffffffffu, near_n, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    if (mis) atomicAdd(counts, mis);
+    if (near_n) atomicAdd(counts + 1, near_n);
+  }
+}
+
 }  // namespace sdk
 
 extern "C" int sd_philox_launch(int n, const uint32_t* ctr, uint64_t seed, uint32_t* out,
@@ -76,6 +102,19 @@ extern "C" int sd_approx_error_launch(uint32_t w_begin, uint64_t count, float* m
   cfg.stream = stream;
   return cudaLaunchKernelEx(&cfg, sdk::approx_error_kernel, w_begin,
                             (unsigned long long)count, max_rel) == cudaSuccess
+             ? SD_OK
+             : SD_E_LAUNCH;
+}
+
+extern "C" int sd_E_check_launch(uint32_t w_begin, uint64_t count, unsigned long long* counts,
+                                 cudaStream_t stream) {
+  if (count == 0) return SD_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(152 * 8, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, sdk::E_check_kernel, w_begin, (unsigned long long)count,
+                            counts) == cudaSuccess
              ? SD_OK
              : SD_E_LAUNCH;
 }
