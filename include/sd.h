@@ -62,6 +62,9 @@ extern "C" {
 #define SD_ERR_MAP_RANGE 8      /* hidden_map row >= n_in_rows: h_shared written instead */
 #define SD_ERR_ZERO_ROW 16      /* a race row without a positive key even on p: token 0 */
 #define SD_ERR_TOTAL_RANGE 32   /* total_out outside [0, capacity]: clamped */
+#define SD_ERR_WAIT 64          /* sd_verify_prepare: a request's first drafter slot was not
+                                   published within the bounded wait; its final token is not
+                                   written to input_ids */
 #define SD_ERR_DRAFT_COUNT 128  /* cu_drafts gives a request a draft count outside [0, K_max]:
                                    clamped (sd_verify_ragged) */
 
@@ -264,6 +267,48 @@ SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int3
                              int H, const void* target_hidden, long ld_in, int n_in_rows,
                              const void* h_shared, void* out_hidden, long ld_out, int32_t* err,
                              void* stream);
+
+/*
+ * sd_verify_prepare -- one step of the hot path in one call: sd_verify followed by
+ * sd_pdraft_prepare on its outputs.
+ *
+ * The two operations are those of sd_verify (speculative-decoding explainer, sections "核心思想"
+ * and "修正拒绝采样") and sd_pdraft_prepare (P-EAGLE blog, sections "Triton Kernel" and "Hidden
+ * State 管理"), with sd_verify's out_tokens and num_accepted feeding the rebuild. When every
+ * request samples (temperature NULL) on probability rows and the batch fits one wave of CTAs,
+ * both run in a single launch: B extra CTAs rebuild the drafter batch while the others race.
+ * A rebuild CTA recomputes the accept decisions of its request and of those before it (they
+ * depend on the inputs only), takes its first drafter slot as their prefix, and writes its
+ * request's rows and hidden states; only the final token at slot a_r waits for the race, and the
+ * CTA that completes request r's race row writes it at the slot the rebuild CTA published in the
+ * workspace (a bounded wait, never taken in practice: the slot appears microseconds after the
+ * launch starts, the race rows complete tens of microseconds later). Other batches run the two
+ * kernels back to back. Either way every output is bit for bit what sd_verify then
+ * sd_pdraft_prepare write.
+ *
+ * Arguments: sd_verify's (without cu_drafts) then sd_pdraft_prepare's from pos0 on (out_tokens
+ * and num_accepted are this call's own outputs), with one workspace of at least
+ * sd_verify_prepare_workspace_bytes(B) bytes (as much as sd_verify's), 16-byte aligned, zeroed
+ * before first use and left zeroed by every call. Errors: those of both calls; SD_ERR_WAIT if a
+ * request's published slot never appeared (its final token is then not written).
+ */
+SD_API int sd_verify_prepare(
+    int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
+    const int32_t* drafts, const float* temperature, uint64_t seed, uint32_t request_base,
+    int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+    const int32_t* pos0, const int32_t* block_table, int max_blocks, int block_size,
+    int32_t mask_token_id, int capacity, int32_t* input_ids, int32_t* positions,
+    int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
+    int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
+    const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
+    long ld_out, void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
+
+/* Workspace of sd_verify_prepare: sd_verify's merge slots, one per request. */
+SD_API size_t sd_verify_prepare_workspace_bytes(int B);
+
+/* Kernels one sd_verify_prepare call with these sizes launches (0, 1 fused, or 2); a planning
+ * query like sd_verify_kernels. */
+SD_API int sd_verify_prepare_kernels(int B, int K, int V, int dtype, int has_temperature);
 
 /*
  * sd_pdraft_prepare_ragged -- sd_pdraft_prepare with a draft count per request, the rebuild

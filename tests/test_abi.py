@@ -87,3 +87,32 @@ def test_host_argument_checks(lib):
     one = ctypes.c_int32(0)
     assert lib.sd_hidden_gather(4, 8, ctypes.addressof(one), 16, 17, 8, 1, 32, 64, 8, P, P) == -4
     assert lib.sd_status_string(-4).decode().startswith("a pointer")
+
+
+def _vp_args(B=4, K=2, V=10, ws_bytes=80, P=16, **over):
+    """sd_verify_prepare's 42 arguments with every pointer set to a dummy non-null value."""
+    a = dict(B=B, K=K, V=V, dtype=0, target=P, ld_t=V, draft=P, ld_d=V, drafts=P, temperature=None,
+             seed=0, request_base=0, out_tokens=P, num_accepted=P, p_at=None, q_at=None, pos0=P,
+             block_table=P, max_blocks=4, block_size=16, mask_id=V, capacity=B * 2 * K,
+             input_ids=P, positions=P, slot_mapping=P, hidden_map=P, is_masked=P, is_rejected=P,
+             start_loc=P, new_token_idx=P, total_out=P, H=8, target_hidden=P, ld_in=8,
+             n_in_rows=B * (K + 1), h_shared=P, out_hidden=P, ld_out=8, workspace=P,
+             ws_bytes=ws_bytes, err=None, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+def test_verify_prepare_host_checks(lib):
+    assert lib.sd_verify_prepare_workspace_bytes(64) == 64 * 16
+    assert lib.sd_verify_prepare_workspace_bytes(0) == 0
+    assert lib.sd_verify_prepare(*_vp_args(K=0)) == -2
+    assert lib.sd_verify_prepare(*_vp_args(dtype=5)) == -3
+    assert lib.sd_verify_prepare(*_vp_args(ws_bytes=63)) == -2        # B*16 needed
+    assert lib.sd_verify_prepare(*_vp_args(H=0)) == -2
+    assert lib.sd_verify_prepare(*_vp_args(h_shared=None)) == -1
+    assert lib.sd_verify_prepare(*_vp_args(start_loc=None)) == -1
+    assert lib.sd_verify_prepare(*_vp_args(target=None)) == -1
+    assert lib.sd_verify_prepare(*_vp_args(workspace=24, ws_bytes=96)) == -4  # 16-byte aligned
+    assert lib.sd_verify_prepare_kernels(4, 2, 10, 7, 0) == -3
+    assert lib.sd_verify_prepare_kernels(4, 0, 10, 0, 0) == -2
+    assert lib.sd_verify_prepare_kernels(0, 2, 10, 0, 0) == 0

@@ -1,0 +1,132 @@
+"""GPU parity of sd_verify_prepare (verify and the drafter-batch rebuild in one call): every
+output bit for bit what sd_verify then sd_pdraft_prepare write on the same inputs, on the fused
+one-launch path (all-sampled probability batches that fit one wave) and on the two-kernel path;
+the workspace is left zeroed; error bits agree; the rebuild matches the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import verify_draft_prep_gb300 as sd
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+REBUILD = ("input_ids", "positions", "slot_mapping", "hidden_map", "is_masked", "is_rejected",
+           "start_loc", "new_token_idx", "total_out")
+
+
+def outputs(w, cap):
+    B, K, dev = w.B, w.K, "cuda"
+    o = dict(out_tokens=torch.full((B, K + 1), 77, dtype=torch.int32, device=dev),
+             num_accepted=torch.full((B,), 77, dtype=torch.int32, device=dev),
+             p_at_draft=torch.full((B, K), 77.0, device=dev),
+             q_at_draft=torch.full((B, K), 77.0, device=dev),
+             input_ids=torch.full((cap,), 77, dtype=torch.int32, device=dev),
+             positions=torch.full((cap,), 77, dtype=torch.int32, device=dev),
+             slot_mapping=torch.full((cap,), 77, dtype=torch.int32, device=dev),
+             hidden_map=torch.full((cap,), 77, dtype=torch.int32, device=dev),
+             is_masked=torch.full((cap,), 77, dtype=torch.uint8, device=dev),
+             is_rejected=torch.full((B, K + 1), 77, dtype=torch.uint8, device=dev),
+             start_loc=torch.full((B + 1,), 77, dtype=torch.int32, device=dev),
+             new_token_idx=torch.full((B, K), 77, dtype=torch.int32, device=dev),
+             total_out=torch.full((1,), 77, dtype=torch.int32, device=dev),
+             out_hidden=torch.full((cap, w.H), 7.0, device=dev).to(torch.bfloat16),
+             err=torch.zeros(1, dtype=torch.int32, device=dev))
+    return o
+
+
+def run_fused(w, T, cap, ws, hidden=None, table=None):
+    o = outputs(w, cap)
+    hidden = w.hidden if hidden is None else hidden
+    table = w.block_table if table is None else table
+    sd.sd_verify_prepare(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"], w.pos0,
+                         table, w.block_size, w.mask_token_id, o["input_ids"], o["positions"],
+                         o["slot_mapping"], o["hidden_map"], o["is_masked"], o["is_rejected"],
+                         o["start_loc"], o["new_token_idx"], o["total_out"], hidden, w.h_shared,
+                         o["out_hidden"], temperature=T, seed=w.seed, p_at_draft=o["p_at_draft"],
+                         q_at_draft=o["q_at_draft"], err=o["err"], workspace_buf=ws)
+    torch.cuda.synchronize()
+    return o
+
+
+def run_separate(w, T, cap, hidden=None, table=None):
+    o = outputs(w, cap)
+    hidden = w.hidden if hidden is None else hidden
+    table = w.block_table if table is None else table
+    sd.sd_verify(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"], temperature=T,
+                 seed=w.seed, p_at_draft=o["p_at_draft"], q_at_draft=o["q_at_draft"],
+                 err=o["err"])
+    sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, table, w.block_size,
+                         w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
+                         o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
+                         o["new_token_idx"], o["total_out"], hidden, w.h_shared, o["out_hidden"],
+                         err=o["err"])
+    torch.cuda.synchronize()
+    return o
+
+
+def assert_same(a, b):
+    for k, v in a.items():
+        x, y = v, b[k]
+        if v.dtype == torch.bfloat16:
+            x, y = v.view(torch.int16), b[k].view(torch.int16)
+        assert torch.equal(x, y), k
+
+
+def new_ws(B):
+    n = sd.load().sd_verify_prepare_workspace_bytes(B)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("name,B,temp,kernels", [
+    ("b64", 64, False, 1),      # the benchmark's workload: one launch
+    ("b64", 16, False, 1),      # more CTAs per request
+    ("small", 1, False, 1),     # one CTA
+    ("b64", 64, True, 2),       # per-request temperatures: verify kernel, then rebuild kernel
+    ("b256mix", 32, True, 2),   # greedy requests among them
+    ("b512rag", 200, False, 2),  # two waves: the race kernel, then the rebuild kernel
+])
+def test_same_bytes_as_the_two_calls(name, B, temp, kernels):
+    w = workloads.make(name, device="cuda", B=B)
+    T = w.temperature if temp else None
+    assert sd.sd_verify_prepare_kernels(w.B, w.K, w.V, sd.SD_F32_PROBS, temp) == kernels
+    ws = new_ws(w.B)
+    want = run_separate(w, T, w.capacity)
+    for _ in range(2):  # the workspace comes back zeroed and serves the next call
+        got = run_fused(w, T, w.capacity, ws)
+        assert_same(got, want)
+        assert int(ws.count_nonzero()) == 0
+    assert int(got["err"].item()) == 0
+
+
+def test_rebuild_matches_the_oracle():
+    w = workloads.make("b64", device="cuda", B=24)
+    got = run_fused(w, None, w.capacity, new_ws(w.B))
+    toks, acc = got["out_tokens"].cpu().numpy(), got["num_accepted"].cpu().numpy()
+    e = oracle.pdraft_expand(toks, acc, w.pos0.cpu().numpy(), w.block_table.cpu().numpy(),
+                             w.block_size, w.mask_token_id)
+    for k in REBUILD:
+        assert np.array_equal(got[k].cpu().numpy(), e[k]), k
+    bits = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    init = torch.full((w.capacity, w.H), 7.0).to(torch.bfloat16)
+    want, gerr = oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], bits(w.hidden),
+                                      bits(w.h_shared), out_init=bits(init))
+    assert gerr == 0 and e["err"] == 0
+    assert np.array_equal(bits(got["out_hidden"]), want)
+
+
+def test_error_paths_match_the_two_calls():
+    w = workloads.make("b64", device="cuda", B=32)
+    table = w.block_table.clone()
+    table[3, :] = -1                      # request 3's slots miss the table
+    n_in = w.B * (w.K + 1) - 5            # the last request's late hidden rows are missing
+    hidden = w.hidden[:n_in]
+    cap = w.B * w.K                       # too small for every outcome
+    for T in (None, w.temperature):
+        want = run_separate(w, T, cap, hidden=hidden, table=table)
+        got = run_fused(w, T, cap, new_ws(w.B), hidden=hidden, table=table)
+        assert_same(got, want)
+        err = int(got["err"].item())
+        assert err & sd.SD_ERR_BLOCK_TABLE and err & sd.SD_ERR_TOTAL_RANGE

@@ -31,6 +31,13 @@ int sd_philox_launch(int, const uint32_t*, uint64_t, uint32_t*, cudaStream_t);
 int sd_race_E_launch(int, const uint32_t*, float*, cudaStream_t);
 int sd_approx_error_launch(uint32_t, uint64_t, float*, cudaStream_t);
 int sd_E_check_launch(uint32_t, uint64_t, unsigned long long*, cudaStream_t);
+int sd_verify_prepare_launch(int, int, int, int, const void*, long, const void*, long,
+                             const int32_t*, const float*, uint64_t, uint32_t, int32_t*, int32_t*,
+                             float*, float*, const int32_t*, const int32_t*, int, int, int32_t,
+                             int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
+                             int32_t*, int32_t*, int32_t*, int, const void*, long, int,
+                             const void*, void*, long, void*, int32_t*, cudaStream_t);
+int sd_verify_prepare_kernel_count(int, int, int, int, int);
 }
 
 namespace {
@@ -350,6 +357,74 @@ int sd_race_E_check(uint32_t w_begin, uint64_t count, uint64_t* counts, void* st
   if (dev != SD_OK) return dev;
   return sd_E_check_launch(w_begin, count, reinterpret_cast<unsigned long long*>(counts),
                            (cudaStream_t)stream);
+}
+
+size_t sd_verify_prepare_workspace_bytes(int B) {
+  return B > 0 ? sd_verify_workspace_launch(B) : 0;
+}
+
+int sd_verify_prepare_kernels(int B, int K, int V, int dtype, int has_temperature) {
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K < 1 || K > SD_K_MAX || V < 1) return SD_E_SHAPE;
+  if (B == 0) return 0;
+  const int dev = check_device();
+  if (dev != SD_OK) return dev;
+  return sd_verify_prepare_kernel_count(B, K, V, dtype, has_temperature);
+}
+
+int sd_verify_prepare(int B, int K, int V, int dtype, const void* target, long ld_t,
+                      const void* draft, long ld_d, const int32_t* drafts,
+                      const float* temperature, uint64_t seed, uint32_t request_base,
+                      int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft,
+                      float* q_at_draft, const int32_t* pos0, const int32_t* block_table,
+                      int max_blocks, int block_size, int32_t mask_token_id, int capacity,
+                      int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
+                      int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
+                      int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
+                      const void* target_hidden, long ld_in, int n_in_rows,
+                      const void* h_shared, void* out_hidden, long ld_out, void* workspace,
+                      size_t workspace_bytes, int32_t* err, void* stream) {
+  // sd_verify's checks
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
+  if ((long long)B * (K + 1) > 2147483647LL) return SD_E_SHAPE;
+  if ((unsigned long long)request_base + (unsigned long long)B > 4294967296ULL) return SD_E_SHAPE;
+  // sd_pdraft_prepare's checks (on this call's own out_tokens / num_accepted)
+  int rc = check_expand_args(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks,
+                             block_size, capacity, input_ids, positions, slot_mapping, hidden_map,
+                             is_masked, is_rejected, start_loc, new_token_idx, total_out);
+  if (rc != SD_OK) return rc;
+  if (H < 1 || ld_in < H || ld_out < H || n_in_rows < 0) return SD_E_SHAPE;
+  if (!h_shared || (capacity > 0 && !out_hidden) || (n_in_rows > 0 && !target_hidden))
+    return SD_E_NULL;
+  if ((uintptr_t)target_hidden % 2 || (uintptr_t)h_shared % 2 || (uintptr_t)out_hidden % 2)
+    return SD_E_ALIGN;
+  if (B == 0) {
+    // no request: the rebuild still reports an empty batch
+    rc = check_device();
+    if (rc != SD_OK) return rc;
+    return sd_prep_launch(0, K, out_tokens, num_accepted, nullptr, pos0, block_table, max_blocks,
+                          block_size, mask_token_id, capacity, input_ids, positions,
+                          slot_mapping, hidden_map, is_masked, is_rejected, start_loc,
+                          new_token_idx, total_out, H, target_hidden, ld_in, n_in_rows, h_shared,
+                          capacity == 0 ? nullptr : out_hidden, ld_out, err,
+                          (cudaStream_t)stream);
+  }
+  if (!target || !draft || !drafts || !workspace) return SD_E_NULL;
+  if (workspace_bytes < sd_verify_prepare_workspace_bytes(B)) return SD_E_SHAPE;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  if ((uintptr_t)target % esize || (uintptr_t)draft % esize) return SD_E_ALIGN;
+  if ((uintptr_t)workspace % 16) return SD_E_ALIGN;
+  rc = check_device();
+  if (rc != SD_OK) return rc;
+  return sd_verify_prepare_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature,
+                                  seed, request_base, out_tokens, num_accepted, p_at_draft,
+                                  q_at_draft, pos0, block_table, max_blocks, block_size,
+                                  mask_token_id, capacity, input_ids, positions, slot_mapping,
+                                  hidden_map, is_masked, is_rejected, start_loc, new_token_idx,
+                                  total_out, H, target_hidden, ld_in, n_in_rows, h_shared,
+                                  capacity == 0 ? nullptr : out_hidden, ld_out, workspace, err,
+                                  (cudaStream_t)stream);
 }
 
 }  // extern "C"

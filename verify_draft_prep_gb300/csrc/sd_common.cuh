@@ -327,6 +327,9 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
 }
 
 // Error bits are rare; one atomic per affected request.
+// Polls a spin-wait may make before it gives up (SD_ERR_WAIT).
+constexpr uint32_t kWaitLimit = 1u << 20;
+
 __device__ __forceinline__ void raise_err(int32_t* err, int32_t bits) {
   if (err && bits) atomicOr(err, bits);
 }

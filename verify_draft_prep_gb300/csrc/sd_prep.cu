@@ -20,7 +20,7 @@
 // kernel is scheduled while sd_verify finishes; it loads the inputs sd_verify does not write
 // (positions) and then waits (griddepcontrol.wait) until sd_verify's results are visible.
 
-#include "sd_common.cuh"
+#include "sd_rebuild.cuh"
 
 namespace sdk {
 
@@ -58,22 +58,6 @@ struct PrepParams {
   int vec;
   int32_t* err;
 };
-
-// One warp copies a row of nv 16-byte words: each lane issues all of its loads (up to
-// kCopyBatch) before its stores, so a row of a few KB costs one memory round trip.
-constexpr int kCopyBatch = 12;
-__device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src,
-                                              uint4* __restrict__ dst, int nv, int lane) {
-  for (int v0 = lane; v0 < nv; v0 += 32 * kCopyBatch) {
-    uint4 x[kCopyBatch];
-#pragma unroll
-    for (int k = 0; k < kCopyBatch; ++k)
-      if (v0 + 32 * k < nv) x[k] = __ldg(src + v0 + 32 * k);
-#pragma unroll
-    for (int k = 0; k < kCopyBatch; ++k)
-      if (v0 + 32 * k < nv) dst[v0 + 32 * k] = x[k];
-  }
-}
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -223,20 +207,11 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
       e |= SD_ERR_TOTAL_RANGE;
       continue;
     }
-    const long long pos = (long long)s_pos[q] + 1 + j;
-    const long long blk = pos >= 0 ? pos / P.block_size : -1;
-    const bool blk_ok = blk >= 0 && blk < P.max_blocks;
     const int32_t tok = (j <= a) ? P.out_tokens[(size_t)rq * (K + 1) + j] : P.mask_id;
-    const long long phys = blk_ok ? (long long)__ldg(P.block_table + (size_t)rq * P.max_blocks + blk) : -1;
-    int32_t slot = -1;
-    const long long sl = phys * P.block_size + pos % P.block_size;
-    if (!blk_ok || phys < 0 || sl > 2147483647LL) e |= SD_ERR_BLOCK_TABLE;
-    else slot = (int32_t)sl;
-    P.input_ids[g] = tok;
-    P.positions[g] = (int32_t)pos;
-    P.slot_mapping[g] = slot;
-    P.hidden_map[g] = (j <= a) ? (int32_t)((long long)s_c0[q] + rq + j) : -1;
-    P.is_masked[g] = (j > a) ? 1 : 0;
+    write_drafter_slot(g, j, a, tok, P.mask_id, s_pos[q],
+                       P.block_table + (size_t)rq * P.max_blocks, P.max_blocks, P.block_size,
+                       (long long)s_c0[q] + rq, P.input_ids, P.positions, P.slot_mapping,
+                       P.hidden_map, P.is_masked, e);
   }
 
   // padding tail [total, capacity), split evenly over the CTAs
@@ -245,13 +220,8 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
     const long long per = (n + gridDim.x - 1) / gridDim.x;
     const long long b0 = tot + per * blockIdx.x;
     const long long b1 = min((long long)P.capacity, b0 + per);
-    for (long long i = b0 + tid; i < b1; i += PNT) {
-      P.input_ids[i] = -1;
-      P.positions[i] = 0;
-      P.slot_mapping[i] = -1;
-      P.hidden_map[i] = -1;
-      P.is_masked[i] = 0;
-    }
+    for (long long i = b0 + tid; i < b1; i += PNT)
+      write_padding_slot(i, P.input_ids, P.positions, P.slot_mapping, P.hidden_map, P.is_masked);
   }
   if (blockIdx.x == 0 && tid == 0) {
     P.start_loc[P.B] = (int32_t)tot;
@@ -271,20 +241,8 @@ __global__ void __launch_bounds__(PNT) prep_kernel(const PrepParams P) {
       }
       const int q = lo, j = (int)i - s_off[q];
       const long long m = (j <= s_a[q]) ? (long long)s_c0[q] + (r0 + q) + j : -1;
-      const uint16_t* src = P.h_shared;
-      if (m >= 0) {
-        if (m < P.n_in_rows) src = P.hidden + m * P.ld_in;
-        else if (lane == 0) e |= SD_ERR_MAP_RANGE;
-      }
-      uint16_t* dst = P.out_hidden + (pre + i) * P.ld_out;
-      if (P.vec) {
-        const int nv = P.H >> 3;
-        const uint4* s4 = reinterpret_cast<const uint4*>(src);
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-        copy_row_warp(s4, d4, nv, lane);
-      } else {
-        for (int x = lane; x < P.H; x += 32) dst[x] = __ldg(src + x);
-      }
+      gather_row_warp(m, P.hidden, P.ld_in, P.n_in_rows, P.h_shared,
+                      P.out_hidden + (pre + i) * P.ld_out, P.H, P.vec != 0, lane, e);
     }
   }
 

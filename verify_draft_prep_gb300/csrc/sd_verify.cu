@@ -34,12 +34,14 @@
 
 #include <float.h>
 #include <math.h>
+#include <string.h>
 
 #include <algorithm>
 #include <atomic>
 #include <type_traits>
 
 #include "sd_common.cuh"
+#include "sd_rebuild.cuh"
 
 namespace sdk {
 
@@ -66,7 +68,34 @@ constexpr float kSkip = (1.0f + kBand) * (1.0f + 0x1p-9f);
 struct RaceSlot {
   unsigned long long best;
   unsigned int count;
-  unsigned int pad;
+  unsigned int off1;  // fused rebuild: request r's first drafter slot + 1 once written, else 0
+};
+
+// The drafter-batch rebuild fused into the verify launch (sd_verify_prepare): the same outputs
+// as the rebuild kernel, written by one extra CTA per request while the others race.
+struct RebuildArgs {
+  const int32_t* pos0;
+  const int32_t* block_table;
+  int max_blocks, block_size;
+  int32_t mask_id;
+  int capacity;
+  int32_t* input_ids;
+  int32_t* positions;
+  int32_t* slot_mapping;
+  int32_t* hidden_map;
+  uint8_t* is_masked;
+  uint8_t* is_rejected;
+  int32_t* start_loc;
+  int32_t* new_token_idx;
+  int32_t* total_out;
+  int H;
+  const uint16_t* hidden;
+  long ld_in;
+  int n_in_rows;
+  const uint16_t* h_shared;
+  uint16_t* out_hidden;  // nullptr: metadata only
+  long ld_out;
+  int hvec;              // 16-byte aligned hidden rows, H a multiple of 8
 };
 
 struct VerifyParams {
@@ -92,6 +121,9 @@ struct VerifyParams {
   int race_blocks;     // blocks after them take the race role (0: sampled requests stay per
                        // request in the cluster role)
   int vec;  // 1: every row starts on a 16-byte boundary
+  int fuse;  // 1: CTAs [0, B) rebuild the drafter batch, CTAs [B, grid) race (spread over the
+             // requests as evenly as they go)
+  RebuildArgs rb;
 };
 
 // Request r's rows: K_r drafts (cu[r+1] - cu[r] when per-request counts are given, clamped to
@@ -1025,26 +1057,33 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
 // Accept scan of request r by one warp (lane j checks draft d_{j+1}); P/Q of the examined drafts
 // go to Ps/Qs (others stay as they are). Returns a_r; *bad_out receives SD_ERR_TOKEN_RANGE when
 // the first rejection came from an out-of-range draft.
+// Whether draft j of request r (rows rr, probability rows) is accepted: d_{j+1} in [0, V) and
+// u_j * Q < P, compared exactly in double (u*Q is exact there). P, Q: the values at the draft
+// (0 for an out-of-range token, which sets bad and counts as rejected).
+__device__ __forceinline__ bool draft_accepted(const VerifyParams& P, const ReqRows& rr, int r,
+                                               int j, float& Pv, float& Qv, bool& bad) {
+  const uint32_t V = (uint32_t)P.V;
+  Pv = 0.0f;
+  Qv = 0.0f;
+  bad = false;
+  const int d = __ldg(P.drafts + rr.d0 + j);
+  if (d < 0 || (uint32_t)d >= V) {
+    bad = true;
+    return false;
+  }
+  Pv = __ldg((const float*)P.target + (rr.t0 + j) * P.ld_t + d);
+  Qv = __ldg((const float*)P.draft + (rr.d0 + j) * P.ld_d + d);
+  const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
+  return u * (double)Qv < (double)Pv;
+}
+
 __device__ int accept_scan_warp(const VerifyParams& P, int r, float* Ps, float* Qs, int* bad_out) {
   const ReqRows rr = req_rows(P, r);
   const int K = rr.k;
-  const uint32_t V = (uint32_t)P.V;
   const int j = threadIdx.x & 31;
-  const float* trow = (const float*)P.target + (rr.t0 + j) * P.ld_t;
-  const float* drow = (const float*)P.draft + (rr.d0 + j) * P.ld_d;
   bool acc = false, bad = false;
   float Pv = 0.0f, Qv = 0.0f;
-  if (j < K) {
-    const int d = __ldg(P.drafts + rr.d0 + j);
-    if (d >= 0 && (uint32_t)d < V) {
-      Pv = __ldg(trow + d);
-      Qv = __ldg(drow + d);
-      const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
-      acc = u * (double)Qv < (double)Pv;  // u*Q is exact in double
-    } else {
-      bad = true;
-    }
-  }
+  if (j < K) acc = draft_accepted(P, rr, r, j, Pv, Qv, bad);
   const unsigned rej = __ballot_sync(0xffffffffu, j < K && !acc);
   const int av = rej ? __ffs(rej) - 1 : K;
   if (j < K && j <= av) {
@@ -1101,7 +1140,7 @@ __device__ bool merge_slot(RaceSlot* slot, uint64_t pk, uint32_t units, uint32_t
 }
 
 // The CTA that completed request r's race row: fallback and outputs, then the slot is zeroed.
-__device__ __noinline__ void finish_sampled(const VerifyParams& P, int r, int a, int32_t e,
+__device__ __noinline__ uint32_t finish_sampled(const VerifyParams& P, int r, int a, int32_t e,
                                             uint64_t pk,
                                const float* Ps, const float* Qs, Smem& sm) {
   const ReqRows rr = req_rows(P, r);
@@ -1124,6 +1163,115 @@ __device__ __noinline__ void finish_sampled(const VerifyParams& P, int r, int a,
     P.slots[r].count = 0u;
   }
   write_request(P, r, a, b, e, Ps, Qs);
+  return b;
+}
+
+// ------------------------------------------------------------------------- fused rebuild
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Sum over the CTA (every thread gets it).
+__device__ long long block_sum_ll(long long v, Smem& sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();  // sm.red may still be read by a previous reduction
+  if ((threadIdx.x & 31) == 0) sm.red[threadIdx.x >> 5] = (uint64_t)v;
+  __syncthreads();
+  long long t = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) t += (long long)sm.red[w];
+  return t;
+}
+
+// Largest batch the fused rebuild takes: every rebuild CTA redoes the accept scans of the
+// requests before its own (kMaxFuseB * SD_K_MAX draft decisions at most, two loads each).
+constexpr int kMaxFuseB = 192;
+
+// The rebuild role of request r (sd_verify_prepare, CTA r of the launch). It needs the accepted
+// counts of requests 0..r, which depend only on the inputs: it recomputes them (the same
+// decisions as the accept scan, all drafts at once), takes its request's first drafter slot as
+// their prefix, and writes r's drafter rows and hidden states -- all while the other CTAs race.
+// Only the final token at slot a_r waits for the race: the CTA that completes r's race row writes
+// it, at the slot this CTA publishes in r's merge slot. The rebuild CTA of the last request also
+// writes total_out, start_loc[B] and the padding tail.
+__device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm) {
+  __shared__ int acc_s[kMaxFuseB];
+  const RebuildArgs& R = P.rb;
+  const int K = P.K, n = r + 1;
+  for (int q = threadIdx.x; q < n; q += NT) acc_s[q] = K;
+  __syncthreads();
+  for (int p = threadIdx.x; p < n * K; p += NT) {
+    const int q = p / K, j = p - q * K;
+    float Pv, Qv;
+    bool bad;
+    if (!draft_accepted(P, req_rows(P, q), q, j, Pv, Qv, bad)) atomicMin(&acc_s[q], j);
+  }
+  __syncthreads();
+  long long part = 0;
+  for (int q = threadIdx.x; q < r; q += NT) part += acc_s[q] + K;
+  const long long off = block_sum_ll(part, sm);
+  const int a = acc_s[r], L = a + K;
+  const ReqRows rr = req_rows(P, r);
+  int32_t e = 0;
+  const int pos0 = __ldg(R.pos0 + r);
+  const int32_t* bt_row = R.block_table + (size_t)r * R.max_blocks;
+  for (int j = threadIdx.x; j < L; j += NT) {
+    const long long g = off + j;
+    if (g >= R.capacity) {
+      e |= SD_ERR_TOTAL_RANGE;
+      continue;
+    }
+    // slot a_r's token is the race's result: its CTA writes it (the tail of the race role)
+    const int32_t tok = j < a ? __ldg(P.drafts + rr.d0 + j) : R.mask_id;
+    write_drafter_slot(g, j, a, tok, R.mask_id, pos0, bt_row, R.max_blocks, R.block_size,
+                       (long long)rr.t0, j == a ? nullptr : R.input_ids, R.positions,
+                       R.slot_mapping, R.hidden_map, R.is_masked, e);
+  }
+  const int t = threadIdx.x;
+  if (t <= K) R.is_rejected[(size_t)r * (K + 1) + t] = (t >= 1 && t > a) ? 1 : 0;
+  if (t < K) R.new_token_idx[(size_t)r * K + t] = (int32_t)(off + a + t);
+  if (t == 0) {
+    R.start_loc[r] = (int32_t)off;
+    st_release_u32(&P.slots[r].off1, (unsigned)(off + 1));
+  }
+  if (R.out_hidden) {
+    const long long nrows = min((long long)L, (long long)R.capacity - off);
+    for (long long j = t >> 5; j < nrows; j += NT / 32)
+      gather_row_warp(j <= a ? (long long)rr.t0 + j : -1, R.hidden, R.ld_in, R.n_in_rows,
+                      R.h_shared, R.out_hidden + (off + j) * R.ld_out, R.H, R.hvec != 0, t & 31,
+                      e);
+  }
+  if (r == P.B - 1) {
+    const long long tot = off + L;
+    if (t == 0) {
+      R.start_loc[P.B] = (int32_t)tot;
+      *R.total_out = (int32_t)tot;
+    }
+    for (long long i = tot + t; i < R.capacity; i += NT)
+      write_padding_slot(i, R.input_ids, R.positions, R.slot_mapping, R.hidden_map, R.is_masked);
+  }
+  if (e) raise_err(P.err, e);
+}
+
+// The race role's share of the fused rebuild: the final token of request r at its slot a_r,
+// once the rebuild CTA has published r's first slot (long before any race row completes; the
+// wait is bounded all the same). Thread 0; clears the published slot for the next call.
+__device__ void write_final_token(const VerifyParams& P, int r, int a, uint32_t b) {
+  unsigned v = ld_acquire_u32(&P.slots[r].off1);
+  for (uint32_t it = 0; v == 0u && it < kWaitLimit; ++it) v = ld_acquire_u32(&P.slots[r].off1);
+  if (v == 0u) {
+    raise_err(P.err, SD_ERR_WAIT);
+    return;
+  }
+  const long long g = (long long)v - 1 + a;
+  if (g < P.rb.capacity) P.rb.input_ids[g] = (int32_t)b;
+  P.slots[r].off1 = 0u;
 }
 
 // The race kernel: an all-sampled batch in one launch. The requests' race rows are laid end to
@@ -1194,9 +1342,30 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
   // When launched as a programmatic dependent, wait until the preceding grid's writes (possibly
   // this launch's inputs) are visible; otherwise this returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int nc = P.nc;
-  const uint32_t rank = blockIdx.x % (unsigned)nc;  // this CTA's index within its request
-  const int r = (int)(blockIdx.x / (unsigned)nc);
+  int nc = P.nc;
+  uint32_t rank;  // this CTA's index within its request
+  int r;
+  if constexpr (DT == SD_F32_PROBS) {
+    if (P.fuse) {
+      // sd_verify_prepare's single launch: CTAs [0, B) rebuild the drafter batch, CTAs
+      // [B, grid) race, dealt out to the requests as evenly as they go (request r takes race
+      // CTAs [floor(r G / B), floor((r+1) G / B)) of the G = grid - B)
+      if (blockIdx.x < (unsigned)P.B) {
+        rebuild_role(P, (int)blockIdx.x, sm);
+        return;
+      }
+      const uint64_t G = gridDim.x - (uint64_t)P.B, Bq = (uint64_t)P.B;
+      const uint64_t c = blockIdx.x - (uint64_t)P.B;
+      r = (int)(((c + 1) * Bq - 1) / G);
+      const uint64_t s0 = (uint64_t)r * G / Bq;
+      nc = (int)((uint64_t)(r + 1) * G / Bq - s0);
+      rank = (uint32_t)(c - s0);
+    }
+  }
+  if (!(DT == SD_F32_PROBS && P.fuse)) {
+    rank = blockIdx.x % (unsigned)nc;
+    r = (int)(blockIdx.x / (unsigned)nc);
+  }
   const ReqRows rr = req_rows(P, r);
   const int K = rr.k;    // this request's drafts
   const int KM = P.K;    // the output stride
@@ -1305,8 +1474,10 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
       pk = race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     }
     uint64_t row_max;
-    if (merge_slot(P.slots + r, pk, u1 - u0, NU, sm, row_max))
-      finish_sampled(P, r, a, e, row_max, sm.P, sm.Q, sm);
+    if (merge_slot(P.slots + r, pk, u1 - u0, NU, sm, row_max)) {
+      const uint32_t bf = finish_sampled(P, r, a, e, row_max, sm.P, sm.Q, sm);
+      if (P.fuse && threadIdx.x == 0) write_final_token(P, r, a, bf);
+    }
     writer = false;  // finish_sampled wrote the outputs (in the CTA that completed the row)
   } else {
     // ---- sampled, bf16 logit rows: per row max/sum, decide, race on the rejected row
@@ -1548,16 +1719,47 @@ extern "C" int sd_verify_kernel_count(int B, int V, int dtype, int has_temperatu
   return B == 0 ? 0 : 1;  // the cluster kernel or the race kernel
 }
 
-extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* target, long ld_t,
-                                const void* draft, long ld_d, const int32_t* drafts,
-                                const int32_t* cu_drafts, const float* temperature,
-                                uint64_t seed, uint32_t request_base,
-                                int32_t* out_tokens,
-                                int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
-                                void* workspace, int32_t* err, cudaStream_t stream) {
-  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+// Launch shape of a verify call: cluster size cl, CTAs per request nc, race-kernel CTAs (0: the
+// cluster kernel takes the batch), and whether a rebuild can join the launch (fusable).
+struct VerifyShape {
+  int cl, nc, race_blocks;
+  bool fusable;
+};
+static VerifyShape verify_shape(int B, int V, int dtype, bool has_temperature, bool ragged) {
+  VerifyShape v;
   const int epu = dtype == SD_F32_PROBS ? 4 : 8;
+  v.cl = choose_cluster(V, epu);
+  v.nc = v.cl;  // CTAs per request in the cluster role
+  v.race_blocks = race_grid(B, V, dtype, has_temperature, v.nc);
+  if (v.race_blocks == 0 && dtype == SD_F32_PROBS && !has_temperature) {
+    // every request samples: its CTAs exchange nothing through shared memory, so no cluster is
+    // needed, and each row splits over as many CTAs as fill one wave of kMinBlocksF32 per SM
+    const int nu = (V + 3) / 4;
+    int nc = sdk::kMinBlocksF32 * sm_count() / std::max(B, 1);
+    nc = std::min(nc, std::max(1, nu / (2 * sdk::NT)));
+    v.cl = 1;
+    v.nc = std::max(nc, 1);
+  }
+  // The fused launch: one wave of kMinBlocksF32 CTAs per SM, B of them rebuilding the drafter
+  // batch and at least as many racing (the race CTAs wait for the rebuild CTAs' published slots
+  // only at their very end, and every CTA of the wave is resident from the start).
+  v.fusable = v.race_blocks == 0 && v.cl == 1 && dtype == SD_F32_PROBS && !has_temperature &&
+              !ragged && B <= sdk::kMaxFuseB && 2L * B <= (long)sdk::kMinBlocksF32 * sm_count();
+  return v;
+}
+
+// The verify launch; with rb, the drafter-batch rebuild joins it when the batch takes the
+// one-wave all-sampled path (*fused = true), else the caller launches the rebuild kernel.
+static int verify_launch_impl(int B, int K, int V, int dtype, const void* target, long ld_t,
+                              const void* draft, long ld_d, const int32_t* drafts,
+                              const int32_t* cu_drafts, const float* temperature, uint64_t seed,
+                              uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
+                              float* p_at_draft, float* q_at_draft, void* workspace,
+                              int32_t* err, cudaStream_t stream, const sdk::RebuildArgs* rb,
+                              bool* fused) {
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
   sdk::VerifyParams P;
+  memset(&P, 0, sizeof(P));
   P.B = B;
   P.K = K;
   P.V = V;
@@ -1576,21 +1778,23 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
   P.q_at = q_at_draft;
   P.slots = (sdk::RaceSlot*)workspace;
   P.err = err;
-  P.cl = choose_cluster(V, epu);
-  P.nc = P.cl;  // CTAs per request in the cluster role
-  P.race_blocks = race_grid(B, V, dtype, temperature != nullptr, P.nc);
-  if (P.race_blocks == 0 && dtype == SD_F32_PROBS && temperature == nullptr) {
-    // every request samples: its CTAs exchange nothing through shared memory, so no cluster is
-    // needed, and each row splits over as many CTAs as fill one wave of kMinBlocksF32 per SM
-    const int nu = (V + 3) / 4;
-    int nc = sdk::kMinBlocksF32 * sm_count() / std::max(B, 1);
-    nc = std::min(nc, std::max(1, nu / (2 * sdk::NT)));
-    P.cl = 1;
-    P.nc = std::max(nc, 1);
-  }
+  const VerifyShape shape = verify_shape(B, V, dtype, temperature != nullptr, cu_drafts != nullptr);
+  P.cl = shape.cl;
+  P.nc = shape.nc;
+  P.race_blocks = shape.race_blocks;
   P.cluster_blocks = B * P.nc;  // (unused when the race kernel takes the batch)
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
+  P.fuse = rb != nullptr && shape.fusable;
+  if (P.fuse) {
+    // B rebuild CTAs, then up to one wave's worth of race CTAs, no more per request than a row
+    // splits into (every race CTA gets at least 2 NT units)
+    P.rb = *rb;
+    const long per = std::max(1, ((V + 3) / 4) / (2 * sdk::NT));
+    const long race = std::min((long)sdk::kMinBlocksF32 * sm_count() - B, (long)B * per);
+    P.cluster_blocks = (int)(B + race);
+  }
+  if (fused) *fused = P.fuse != 0;
   if (B == 0) return SD_OK;
 
   cudaLaunchConfig_t cfg = {};
@@ -1631,6 +1835,88 @@ extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* targ
     rc = cudaLaunchKernelEx(&rcfg, sdk::race_kernel, P);
   }
   return rc == cudaSuccess ? SD_OK : SD_E_LAUNCH;
+}
+
+extern "C" int sd_verify_launch(int B, int K, int V, int dtype, const void* target, long ld_t,
+                                const void* draft, long ld_d, const int32_t* drafts,
+                                const int32_t* cu_drafts, const float* temperature,
+                                uint64_t seed, uint32_t request_base, int32_t* out_tokens,
+                                int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+                                void* workspace, int32_t* err, cudaStream_t stream) {
+  return verify_launch_impl(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts,
+                            temperature, seed, request_base, out_tokens, num_accepted,
+                            p_at_draft, q_at_draft, workspace, err, stream, nullptr, nullptr);
+}
+
+extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int32_t* num_accepted,
+                              const int32_t* cu_drafts, const int32_t* pos0,
+                              const int32_t* block_table, int max_blocks, int block_size,
+                              int32_t mask_token_id, int capacity, int32_t* input_ids,
+                              int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map,
+                              uint8_t* is_masked, uint8_t* is_rejected, int32_t* start_loc,
+                              int32_t* new_token_idx, int32_t* total_out, int H,
+                              const void* target_hidden, long ld_in, int n_in_rows,
+                              const void* h_shared, void* out_hidden, long ld_out, int32_t* err,
+                              cudaStream_t stream);
+
+// Verify and rebuild in one call: one launch when the batch takes the one-wave all-sampled path,
+// else the verify kernel and then the rebuild kernel (the same outputs either way). The
+// workspace holds the B merge slots (each also carries its request's first drafter slot from the
+// rebuild CTA to the CTA that writes the final token).
+extern "C" int sd_verify_prepare_launch(
+    int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
+    const int32_t* drafts, const float* temperature, uint64_t seed, uint32_t request_base,
+    int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+    const int32_t* pos0, const int32_t* block_table, int max_blocks, int block_size,
+    int32_t mask_token_id, int capacity, int32_t* input_ids, int32_t* positions,
+    int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
+    int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
+    const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
+    long ld_out, void* workspace, int32_t* err, cudaStream_t stream) {
+  sdk::RebuildArgs rb;
+  rb.pos0 = pos0;
+  rb.block_table = block_table;
+  rb.max_blocks = max_blocks;
+  rb.block_size = block_size;
+  rb.mask_id = mask_token_id;
+  rb.capacity = capacity;
+  rb.input_ids = input_ids;
+  rb.positions = positions;
+  rb.slot_mapping = slot_mapping;
+  rb.hidden_map = hidden_map;
+  rb.is_masked = is_masked;
+  rb.is_rejected = is_rejected;
+  rb.start_loc = start_loc;
+  rb.new_token_idx = new_token_idx;
+  rb.total_out = total_out;
+  rb.H = H;
+  rb.hidden = (const uint16_t*)target_hidden;
+  rb.ld_in = ld_in;
+  rb.n_in_rows = n_in_rows;
+  rb.h_shared = (const uint16_t*)h_shared;
+  rb.out_hidden = (uint16_t*)out_hidden;
+  rb.ld_out = ld_out;
+  rb.hvec = out_hidden && (H % 8 == 0) && ((uintptr_t)target_hidden % 16 == 0) &&
+            ((uintptr_t)h_shared % 16 == 0) && ((uintptr_t)out_hidden % 16 == 0) &&
+            (ld_in % 8 == 0) && (ld_out % 8 == 0);
+  bool fused = false;
+  int rc = verify_launch_impl(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, nullptr,
+                              temperature, seed, request_base, out_tokens, num_accepted,
+                              p_at_draft, q_at_draft, workspace, err, stream, &rb, &fused);
+  if (rc != SD_OK || fused) return rc;
+  return sd_prep_launch(B, K, out_tokens, num_accepted, nullptr, pos0, block_table, max_blocks,
+                        block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
+                        hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out,
+                        H, target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
+                        stream);
+}
+
+// Kernels one sd_verify_prepare call launches.
+extern "C" int sd_verify_prepare_kernel_count(int B, int K, int V, int dtype,
+                                              int has_temperature) {
+  (void)K;
+  if (B == 0) return 0;
+  return verify_shape(B, V, dtype, has_temperature != 0, false).fusable ? 1 : 2;
 }
 
 // ------------------------------------------------------------------ no-allocation entry point
