@@ -38,16 +38,17 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "b4e06989d953523a"): (82.746368e6, "ncu --set full, one launch of the full batch"),
-    ("b256mix", "b4e06989d953523a"): (439.775744e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "b4e06989d953523a"): (783.75895e6, "ncu --set full at B=160, scaled x3.2"),
-    ("b1024lg", "b4e06989d953523a"): (3023.7027e6, "ncu --set full at B=96, scaled x1024/96"),
+    ("b64", "425e31c0b3abb730"): (85.607424e6, "ncu --set full, one fused launch of the full "
+                                               "batch (one input set)"),
+    ("b256mix", "425e31c0b3abb730"): (440.261632e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "425e31c0b3abb730"): (776.221355e6, "ncu --set full at B=192, scaled x512/192"),
+    ("b1024lg", "425e31c0b3abb730"): (3028.62336e6, "ncu --set full at B=96, scaled x1024/96"),
 }
 
 
 def _src_hash():
     h = hashlib.sha256()
-    for f in ("sd_verify.cu", "sd_common.cuh"):
+    for f in ("sd_verify.cu", "sd_common.cuh", "sd_rebuild.cuh"):
         with open(os.path.join(ROOT, "verify_draft_prep_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -192,14 +193,16 @@ def temperatures(w):
 
 
 def launch_step(sd, w, o, stream=None):
-    """One step: verify, then the fused draft-batch rebuild + hidden gather (a programmatic
-    dependent launch of verify)."""
-    launch_verify(sd, w, o, stream)
-    sd.sd_pdraft_prepare(o["out_tokens"], o["num_accepted"], w.pos0, w.block_table, w.block_size,
-                         w.mask_token_id, o["input_ids"], o["positions"], o["slot_mapping"],
-                         o["hidden_map"], o["is_masked"], o["is_rejected"], o["start_loc"],
-                         o["new_token_idx"], o["total_out"], w.hidden, w.h_shared,
-                         o["out_hidden"], err=o["err"], stream=stream)
+    """One step through sd_verify_prepare: verify and the draft-batch rebuild + hidden gather in
+    one launch when every request samples on probability rows and the batch fits one wave, else
+    the verify kernel and the rebuild kernel (its programmatic dependent)."""
+    sd.sd_verify_prepare(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"], w.pos0,
+                         w.block_table, w.block_size, w.mask_token_id, o["input_ids"],
+                         o["positions"], o["slot_mapping"], o["hidden_map"], o["is_masked"],
+                         o["is_rejected"], o["start_loc"], o["new_token_idx"], o["total_out"],
+                         w.hidden, w.h_shared, o["out_hidden"], temperature=temperatures(w),
+                         seed=w.seed, err=o["err"], stream=stream, workspace_buf=o["ws"],
+                         request_base=getattr(w, "request_base", 0))
 
 
 def launch_prepare(sd, w, o, stream=None):
@@ -361,11 +364,6 @@ def main():
         for i in range(args.warmup):
             launch_step(sd, sets[i % nsets], outs[i % nsets], stream)
     stream.synchronize()
-    per_set = []
-    for w, o in zip(sets, outs):
-        a = o["num_accepted"].cpu().numpy()
-        per_set.append(algorithmic_bytes(w, a)[:3] + (a, algorithmic_bytes(w, a)[3]))
-    errs = [int(o["err"].item()) for o in outs]
 
     # the timed steps are replayed from CUDA graphs of up to CHUNK steps (a graph of K % CHUNK
     # steps makes up the rest, so exactly K steps run); the timed region is bracketed by two
@@ -417,8 +415,22 @@ def main():
     if world > 1:
         dist.barrier()
     total_ms = start.elapsed_time(end)
+    # bytes per step from each set's accepted counts (every set has run by now: the graphs
+    # rotate over all of them; the same inputs give the same counts on every run)
+    per_set = []
+    for w, o in zip(sets, outs):
+        a = o["num_accepted"].cpu().numpy()
+        per_set.append(algorithmic_bytes(w, a)[:3] + (a, algorithmic_bytes(w, a)[3]))
+    errs = [int(o["err"].item()) for o in outs]
     step_ms = [evs[s].elapsed_time(evs[s + 1]) for s in range(CHUNK)] if evs else []
-    # the dominant kernel alone, K launches in a graph of its own, right after the timed region
+    # the dominant kernel alone, K launches in a graph of its own, right after the timed region:
+    # the fused step kernel when the step is one launch, else the verify kernel
+    dt_code = 0 if cfg["kind"] == "probs" else 1
+    has_t = temperatures(sets[0]) is not None
+    step_kernels = sd.sd_verify_prepare_kernels(sets[0].B, sets[0].K, sets[0].V, dt_code, has_t)
+    fused = step_kernels == 1
+    avg_f = time_graph(lambda w, o, st: launch_step(sd, w, o, st), sets, outs, stream,
+                       CHUNK) if fused else None
     avg_v = time_graph(lambda w, o, st: launch_verify(sd, w, o, st), sets, outs, stream, CHUNK)
     avg_p = time_graph(lambda w, o, st: launch_prepare(sd, w, o, st), sets, outs, stream, CHUNK)
     # the padded form of the rebuild (fixed 2K-slot rows), timed alone after the same verify
@@ -439,7 +451,11 @@ def main():
     bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(CHUNK)]))
     bytes_read = float(np.mean([per_set[s % nsets][4] for s in range(CHUNK)]))
     peak, peak_kind = _peaks()
-    achieved = bytes_v / (avg_v * 1e-3) / 1e9
+    # roofline of the dominant kernel: the fused step kernel moves the verify's, the expand's and
+    # the gather's bytes; the verify kernel alone the verify's
+    bytes_dom = bytes_all if fused else bytes_v
+    avg_dom = avg_f if fused else avg_v
+    achieved = bytes_dom / (avg_dom * 1e-3) / 1e9
     traffic, traffic_note = (None, "no capture of the current kernel source")
     if not args.batch and (args.config, _src_hash()) in MEASURED_TRAFFIC:
         traffic, traffic_note = MEASURED_TRAFFIC[(args.config, _src_hash())]
@@ -451,9 +467,8 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(host_copy(sets[0]))
 
-    # kernels per step: the verify call's (one, or accept + race) and the fused rebuild's one
-    launches = sd.sd_verify_kernels(B, sets[0].V, 0 if cfg["kind"] == "probs" else 1,
-                                    temperatures(sets[0]) is not None) + 1
+    # kernels per step: one fused launch, or the verify kernel and the rebuild kernel
+    launches = step_kernels
     a_all = np.concatenate([p[3] for p in per_set])
     w0s = sets[0]
     sample_bytes = w0s.B * w0s.K * w0s.V * w0s.draft.element_size() + w0s.B * w0s.K * 4 + w0s.B * 4
@@ -493,19 +508,26 @@ def main():
                        "l2": f"{nsets} rotating input sets (rows of all sets "
                              f"{nsets * sets[0].target.numel() * sets[0].target.element_size() / 1e9:.1f} GB"
                              f" > 129 MB L2; a set recurs after {nsets - 1} others)",
-                       "timing": "one CUDA graph of all timed steps (verify, then the fused "
-                                 "rebuild as its programmatic dependent); the verify kernel "
-                                 "alone in a second graph for the roofline",
+                       "timing": "CUDA graphs of the timed steps, one sd_verify_prepare call "
+                                 "each (one launch when the batch is all-sampled and fits one "
+                                 "wave, else verify then the rebuild as its programmatic "
+                                 "dependent); the dominant kernel alone in a second graph for "
+                                 "the roofline",
                        "parallelism": f"dp{world}: request shards of {B} per GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "traffic_source": traffic_note,
-                         "kernel": "sd_verify", "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": bytes_v,
-                         "bytes_model": "minimum bytes (scalar gathers + one p and one q row "
-                                        "per sampled request, a_r + 1 rows per greedy one)"
-                         if cfg["kind"] == "probs" else
-                         "full rows (2K + 1 logit rows per request)",
+                         "kernel": "sd_verify_prepare (verify and rebuild in one launch)"
+                         if fused else "sd_verify", "kernel_us": avg_dom * 1e3,
+                         "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": bytes_dom,
+                         "bytes_model": ("minimum bytes (scalar gathers + one p and one q row "
+                                         "per sampled request, a_r + 1 rows per greedy one)"
+                                         if cfg["kind"] == "probs" else
+                                         "full rows (2K + 1 logit rows per request)")
+                         + ("; plus the rebuild's slots and hidden rows" if fused else ""),
+                         "verify_alone": {"us": avg_v * 1e3, "bytes": bytes_v,
+                                          "frac": bytes_v / (avg_v * 1e-3) / 1e9 / peak},
                          "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
                          "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * K, "clocks": clk,
