@@ -190,7 +190,6 @@ template <bool HAS_Q>
 struct F32Residual {
   static constexpr int EPU = 4;
   static constexpr int UNR = 2;  // units in flight per thread
-  static constexpr int ROWS = HAS_Q ? 2 : 1;
   const float* p;
   const float* q;
   uint32_t V;
@@ -204,18 +203,6 @@ struct F32Residual {
   }
   // units entirely inside the row, read with unchecked 128-bit loads when vec is set
   __device__ __forceinline__ uint32_t full_units() const { return V / 4u; }
-  __device__ __forceinline__ const uint8_t* row_bytes(int r) const {
-    return (const uint8_t*)(r == 0 ? p : q);
-  }
-  __device__ __forceinline__ void from_smem(const uint8_t* const (&st)[ROWS], uint32_t i,
-                                            Raw& raw) const {
-    const float4 a = *reinterpret_cast<const float4*>(st[0] + 16u * i);
-    raw.p[0] = a.x; raw.p[1] = a.y; raw.p[2] = a.z; raw.p[3] = a.w;
-    if (HAS_Q) {
-      const float4 b = *reinterpret_cast<const float4*>(st[ROWS - 1] + 16u * i);
-      raw.q[0] = b.x; raw.q[1] = b.y; raw.q[2] = b.z; raw.q[3] = b.w;
-    }
-  }
   __device__ __forceinline__ void fetch_fast(uint32_t u, Raw& raw) const {
     const float4 a = ld_f4(p + 4u * u);
     raw.p[0] = a.x; raw.p[1] = a.y; raw.p[2] = a.z; raw.p[3] = a.w;
@@ -292,7 +279,6 @@ template <bool HAS_Q>
 struct Bf16Residual {
   static constexpr int EPU = 8;
   static constexpr int UNR = 2;
-  static constexpr int ROWS = HAS_Q ? 2 : 1;
   const uint16_t* t;
   const uint16_t* d;
   float Mt, invSt, Md, invSd, c;
@@ -306,14 +292,6 @@ struct Bf16Residual {
     if (HAS_Q) raw.d = bf16_raw(d, u, V, vec);
   }
   __device__ __forceinline__ uint32_t full_units() const { return V / 8u; }
-  __device__ __forceinline__ const uint8_t* row_bytes(int r) const {
-    return (const uint8_t*)(r == 0 ? t : d);
-  }
-  __device__ __forceinline__ void from_smem(const uint8_t* const (&st)[ROWS], uint32_t i,
-                                            Raw& raw) const {
-    raw.t = *reinterpret_cast<const uint4*>(st[0] + 16u * i);
-    if (HAS_Q) raw.d = *reinterpret_cast<const uint4*>(st[ROWS - 1] + 16u * i);
-  }
   __device__ __forceinline__ void fetch_fast(uint32_t u, Raw& raw) const {
     raw.t = ld_stream_u4(t + 8u * u);
     if (HAS_Q) raw.d = ld_stream_u4(d + 8u * u);
