@@ -87,6 +87,8 @@ def new_ws(B):
     ("b64", 64, True, 2),       # per-request temperatures: verify kernel, then rebuild kernel
     ("b256mix", 32, True, 2),   # greedy requests among them
     ("b512rag", 200, False, 2),  # two waves: the race kernel, then the rebuild kernel
+    ("small", 192, False, 1),   # the largest batch the single launch takes
+    ("small", 193, False, 2),   # one more request: two kernels
 ])
 def test_same_bytes_as_the_two_calls(name, B, temp, kernels):
     w = workloads.make(name, device="cuda", B=B)
