@@ -278,7 +278,7 @@ __device__ __forceinline__ float logit_prob(float l, float M, float c, float inv
 template <bool HAS_Q>
 struct Bf16Residual {
   static constexpr int EPU = 8;
-  static constexpr int UNR = 2;
+  static constexpr int UNR = 1;  // one unit in flight: no spills at the kernel's 64 registers
   const uint16_t* t;
   const uint16_t* d;
   float Mt, invSt, Md, invSd, c;
