@@ -1590,7 +1590,9 @@ struct SampleParams {
 };
 
 template <int DT>
-__global__ void __launch_bounds__(NT, kMinBlocks) sample_kernel(const __grid_constant__ SampleParams P) {
+// (fp32 rows at the verify kernel's 5 CTAs per SM: 4 to 6% faster than at 4 despite a few spills)
+__global__ void __launch_bounds__(NT, min_blocks(DT))
+    sample_kernel(const __grid_constant__ SampleParams P) {
   __shared__ Smem sm;
   constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
   asm volatile("griddepcontrol.wait;" ::: "memory");
