@@ -664,7 +664,7 @@ __device__ uint64_t race_chunk_log(const uint16_t* row, uint32_t V, bool vec, fl
   uint32_t best_u = 0xffffffffu;
   const uint32_t uf = vec ? max(u0, min(u1, V / 8u)) : u0;
   uint32_t ub = u0 + threadIdx.x;
-  constexpr int UNR = 2;
+  constexpr int UNR = 1;  // one unit in flight: the sampler fits 5 CTAs per SM unspilled
   if (ub + (UNR - 1) * NT < uf) {
     uint4 raw[UNR];
 #pragma unroll
@@ -1590,8 +1590,9 @@ struct SampleParams {
 };
 
 template <int DT>
-// (fp32 rows at the verify kernel's 5 CTAs per SM: 4 to 6% faster than at 4 despite a few spills)
-__global__ void __launch_bounds__(NT, min_blocks(DT))
+// 5 CTAs per SM (48 registers): fp32 rows 1.4 to 6% faster than at 4 despite a few spills,
+// logit rows (one unit in flight, no spills) 6.5% faster
+__global__ void __launch_bounds__(NT, kMinBlocksF32)
     sample_kernel(const __grid_constant__ SampleParams P) {
   __shared__ Smem sm;
   constexpr int EPU = (DT == SD_F32_PROBS) ? 4 : 8;
