@@ -46,14 +46,15 @@
 namespace sdk {
 
 constexpr int NT = 256;        // threads per CTA
-constexpr int UNROLL = 4;      // 16-byte units in flight per thread (greedy rows, statistics)
+constexpr int UNROLL = 3;      // 16-byte units in flight per thread and row (logit statistics)
 constexpr int kArgmaxUnroll = 8;  // the same for greedy argmax rows (loads only: more in flight)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
-constexpr int kMinBlocks = 4;  // resident CTAs per SM the cluster kernel's registers allow
-// the verify kernel on fp32 rows keeps 2 race units in flight per thread and fits 5 CTAs per SM
-// (measured better than 4 CTAs with 4 units for the one-wave and mixed batches); on logit rows
-// the statistics pass needs the registers of 4
+// Resident CTAs per SM of the verify kernel (48 registers). On fp32 rows it keeps 2 race units in
+// flight per thread (measured better than 4 CTAs with 4 units for the one-wave and mixed
+// batches); on logit rows 3 statistics units per row and 1 race unit (measured better than 4
+// CTAs with 4 and 2: more clusters resident).
 constexpr int kMinBlocksF32 = 5;
+constexpr int kMinBlocks = 5;
 constexpr int min_blocks(int dt) { return dt == SD_F32_PROBS ? kMinBlocksF32 : kMinBlocks; }
 constexpr int kRaceMinBlocks = 4;  // the same for race_kernel (its loop keeps 3 units in flight)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
