@@ -47,7 +47,7 @@ namespace sdk {
 
 constexpr int NT = 256;        // threads per CTA
 constexpr int UNROLL = 3;      // 16-byte units in flight per thread and row (logit statistics)
-constexpr int kArgmaxUnroll = 8;  // the same for greedy argmax rows (loads only: more in flight)
+constexpr int kArgmaxUnroll = 6;  // the same for greedy argmax rows (loads only: more in flight)
 constexpr int CL_MAX = 8;      // CTAs per request (portable cluster size)
 // Resident CTAs per SM of the verify kernel (48 registers). On fp32 rows it keeps 2 race units in
 // flight per thread (measured better than 4 CTAs with 4 units for the one-wave and mixed
