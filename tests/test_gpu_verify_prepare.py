@@ -132,3 +132,18 @@ def test_error_paths_match_the_two_calls():
         assert_same(got, want)
         err = int(got["err"].item())
         assert err & sd.SD_ERR_BLOCK_TABLE and err & sd.SD_ERR_TOTAL_RANGE
+
+
+def test_out_of_range_drafts_match_the_two_calls():
+    # a draft token outside [0, V) is rejected with SD_ERR_TOKEN_RANGE; on the single launch the
+    # rebuild CTA, which recomputes the decisions, raises it
+    w = workloads.make("b64", device="cuda", B=16)
+    w.drafts = w.drafts.clone()
+    w.drafts[2, 0] = w.V            # request 2: its first draft is out of range
+    w.drafts[5, 3] = -4             # request 5: its fourth
+    assert sd.sd_verify_prepare_kernels(w.B, w.K, w.V, sd.SD_F32_PROBS, False) == 1
+    want = run_separate(w, None, w.capacity)
+    got = run_fused(w, None, w.capacity, new_ws(w.B))
+    assert_same(got, want)
+    assert int(got["err"].item()) & sd.SD_ERR_TOKEN_RANGE
+    assert int(got["num_accepted"][2]) == 0
