@@ -1119,9 +1119,11 @@ __device__ bool merge_slot(RaceSlot* slot, uint64_t pk, uint32_t units, uint32_t
 }
 
 // The CTA that completed request r's race row: fallback and outputs, then the slot is zeroed.
-__device__ __noinline__ uint32_t finish_sampled(const VerifyParams& P, int r, int a, int32_t e,
-                                            uint64_t pk,
-                               const float* Ps, const float* Qs, Smem& sm) {
+// Request r's final token from its completed race row (maximum pk): the fallback race on p when
+// no residual key is positive, SD_ERR_ZERO_ROW into e when even p has none; the merge slot is
+// cleared for the next call.
+__device__ uint32_t final_token(const VerifyParams& P, int r, int a, uint64_t pk, int32_t& e,
+                                Smem& sm) {
   const ReqRows rr = req_rows(P, r);
   const int K = rr.k;
   const uint32_t V = (uint32_t)P.V;
@@ -1141,16 +1143,18 @@ __device__ __noinline__ uint32_t finish_sampled(const VerifyParams& P, int r, in
     P.slots[r].best = 0ull;
     P.slots[r].count = 0u;
   }
+  return b;
+}
+
+__device__ __noinline__ uint32_t finish_sampled(const VerifyParams& P, int r, int a, int32_t e,
+                                                uint64_t pk, const float* Ps, const float* Qs,
+                                                Smem& sm) {
+  const uint32_t b = final_token(P, r, a, pk, e, sm);
   write_request(P, r, a, b, e, Ps, Qs);
   return b;
 }
 
 // ------------------------------------------------------------------------- fused rebuild
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -1238,19 +1242,36 @@ __device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm
   if (e) raise_err(P.err, e);
 }
 
-// The race role's share of the fused rebuild: the final token of request r at its slot a_r,
-// once the rebuild CTA has published r's first slot (long before any race row completes; the
-// wait is bounded all the same). Thread 0; clears the published slot for the next call.
-__device__ void write_final_token(const VerifyParams& P, int r, int a, uint32_t b) {
-  unsigned v = ld_acquire_u32(&P.slots[r].off1);
-  for (uint32_t it = 0; v == 0u && it < kWaitLimit; ++it) v = ld_acquire_u32(&P.slots[r].off1);
-  if (v == 0u) {
-    raise_err(P.err, SD_ERR_WAIT);
-    return;
+// The CTA that completed request r's race row in the fused launch: the verify outputs (as
+// write_request) and the final token at slot a_r of the drafter batch, at the first slot the
+// rebuild CTA published (long before any race row completes; the wait is bounded all the same).
+// tok_pre (thread t < K: draft t) and off_pre (thread 0: the published slot + 1, or 0 if not yet
+// seen) were read before the merge, so that their round trips overlap the merge's. No acquire is
+// needed: the CTA reads nothing else the rebuild CTA wrote, and writes a slot it leaves alone.
+__device__ __noinline__ void fused_finish(const VerifyParams& P, int r, int a, int32_t e,
+                                          uint64_t pk, const float* Ps, const float* Qs,
+                                          int32_t tok_pre, unsigned off_pre, Smem& sm) {
+  const uint32_t b = final_token(P, r, a, pk, e, sm);
+  const int K = P.K, t = threadIdx.x;
+  if (t <= K) P.out_tokens[(size_t)r * (K + 1) + t] = t < a ? tok_pre : (t == a ? (int32_t)b : -1);
+  if (t < K) {
+    if (P.p_at) P.p_at[(size_t)r * K + t] = Ps[t];
+    if (P.q_at) P.q_at[(size_t)r * K + t] = Qs[t];
   }
-  const long long g = (long long)v - 1 + a;
-  if (g < P.rb.capacity) P.rb.input_ids[g] = (int32_t)b;
-  P.slots[r].off1 = 0u;
+  if (t == 0) {
+    P.num_accepted[r] = a;
+    volatile unsigned* slot = &P.slots[r].off1;
+    unsigned v = off_pre;
+    for (uint32_t it = 0; v == 0u && it < kWaitLimit; ++it) v = *slot;
+    if (v == 0u) {
+      e |= SD_ERR_WAIT;
+    } else {
+      const long long g = (long long)v - 1 + a;
+      if (g < P.rb.capacity) P.rb.input_ids[g] = (int32_t)b;
+      *slot = 0u;
+    }
+    raise_err(P.err, e);
+  }
 }
 
 // The race kernel: an all-sampled batch in one launch. The requests' race rows are laid end to
@@ -1453,9 +1474,16 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
       pk = race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm);
     }
     uint64_t row_max;
+    // fused launch: the final token's inputs, read now so that they arrive during the merge
+    int32_t tok_pre = 0;
+    unsigned off_pre = 0u;
+    if (P.fuse) {
+      if (threadIdx.x < (unsigned)K) tok_pre = __ldg(dr + threadIdx.x);
+      if (threadIdx.x == 0) off_pre = *(volatile unsigned*)&P.slots[r].off1;
+    }
     if (merge_slot(P.slots + r, pk, u1 - u0, NU, sm, row_max)) {
-      const uint32_t bf = finish_sampled(P, r, a, e, row_max, sm.P, sm.Q, sm);
-      if (P.fuse && threadIdx.x == 0) write_final_token(P, r, a, bf);
+      if (P.fuse) fused_finish(P, r, a, e, row_max, sm.P, sm.Q, tok_pre, off_pre, sm);
+      else finish_sampled(P, r, a, e, row_max, sm.P, sm.Q, sm);
     }
     writer = false;  // finish_sampled wrote the outputs (in the CTA that completed the row)
   } else {
