@@ -147,3 +147,39 @@ def test_out_of_range_drafts_match_the_two_calls():
     assert_same(got, want)
     assert int(got["err"].item()) & sd.SD_ERR_TOKEN_RANGE
     assert int(got["num_accepted"][2]) == 0
+
+
+def test_unaligned_rows_and_ragged_vocabulary():
+    # rows that do not start on 16-byte boundaries (scalar loads) and a vocabulary that is not a
+    # multiple of the 4-entry unit: the single launch's race tails, against the two calls
+    rng = np.random.default_rng(11)
+    B, K, V, H = 24, 3, 5003, 40
+    w = workloads.make("small", device="cuda", B=B)
+    lt = 2.0 * rng.standard_normal((B * (K + 1), V))
+    p = np.exp(lt - lt.max(-1, keepdims=True))
+    p = (p / p.sum(-1, keepdims=True)).astype(np.float32)
+    lq = lt[np.arange(B * (K + 1)).reshape(B, K + 1)[:, :K].reshape(-1)] + 0.5 * rng.standard_normal((B * K, V))
+    q = np.exp(lq - lq.max(-1, keepdims=True))
+    q = (q / q.sum(-1, keepdims=True)).astype(np.float32)
+    q64 = q.astype(np.float64)
+    d = np.array([rng.choice(V, p=q64[i] / q64[i].sum()) for i in range(B * K)],
+                 np.int32).reshape(B, K)
+    ld = V + 1                                      # odd row stride: no 16-byte rows
+    tbuf = torch.zeros(B * (K + 1), ld, device="cuda")
+    dbuf = torch.zeros(B * K, ld, device="cuda")
+    tbuf[:, :V] = torch.from_numpy(p).cuda()
+    dbuf[:, :V] = torch.from_numpy(q).cuda()
+    w.target, w.draft = tbuf[:, :V], dbuf[:, :V]
+    w.drafts = torch.from_numpy(d).cuda()
+    w.K, w.V, w.H = K, V, H
+    w.hidden = torch.from_numpy(rng.standard_normal((B * (K + 1), H)).astype(np.float32)).to(
+        torch.bfloat16).cuda()
+    w.h_shared = torch.from_numpy(rng.standard_normal(H).astype(np.float32)).to(torch.bfloat16).cuda()
+    w.mask_token_id = V
+    assert sd.sd_verify_prepare_kernels(B, K, V, sd.SD_F32_PROBS, False) == 1
+    want = run_separate(w, None, w.capacity)
+    got = run_fused(w, None, w.capacity, new_ws(B))
+    assert_same(got, want)
+    assert int(got["err"].item()) == 0
+    ref = oracle.verify_probs(p.reshape(B, K + 1, V), q.reshape(B, K, V), d, seed=w.seed)
+    assert np.array_equal(got["out_tokens"].cpu().numpy(), ref["out_tokens"])
