@@ -303,7 +303,26 @@ SD_API int sd_verify_prepare(
     const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
     long ld_out, void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
 
-/* Workspace of sd_verify_prepare: sd_verify's merge slots, one per request. */
+/*
+ * sd_verify_prepare_ragged -- sd_verify_ragged then sd_pdraft_prepare_ragged on its outputs, in
+ * one call: a draft count per request (cu_drafts [B+1], rows packed as sd_verify_ragged reads
+ * them, K_max the output stride), with the same single launch for all-sampled one-wave batches
+ * (the rebuild CTAs recompute every request's decisions over its own K_r drafts). Every output is
+ * bit for bit what the two ragged calls write; arguments and errors as for them and
+ * sd_verify_prepare.
+ */
+SD_API int sd_verify_prepare_ragged(
+    int B, int K_max, int V, int dtype, const void* target, long ld_t, const void* draft,
+    long ld_d, const int32_t* drafts, const int32_t* cu_drafts, const float* temperature,
+    uint64_t seed, uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
+    float* p_at_draft, float* q_at_draft, const int32_t* pos0, const int32_t* block_table,
+    int max_blocks, int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
+    int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked,
+    uint8_t* is_rejected, int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
+    const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
+    long ld_out, void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
+
+/* Workspace of sd_verify_prepare (and _ragged): sd_verify's merge slots, one per request. */
 SD_API size_t sd_verify_prepare_workspace_bytes(int B);
 
 /* Kernels one sd_verify_prepare call with these sizes launches (0, 1 fused, or 2); a planning

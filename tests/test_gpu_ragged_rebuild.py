@@ -98,3 +98,71 @@ def test_ragged_step_end_to_end():
     gh, _ = oracle.hidden_gather(tot, want["hidden_map"], bits(hid), bits(hs))
     assert np.array_equal(got["out_hidden"][:tot], gh[:tot])
     assert got["err"] == want["err"] == 0
+
+
+@pytest.mark.parametrize("B,K_max,V,greedy,temp,kernels", [
+    (48, 6, 20011, 0.0, False, 1),   # every request samples: the single launch
+    (40, 16, 4099, 0.0, False, 1),   # K_max = SD_K_MAX, counts 0..16
+    (48, 6, 20011, 0.3, True, 2),    # greedy requests among them: two kernels
+])
+def test_one_call_ragged_step(B, K_max, V, greedy, temp, kernels):
+    # sd_verify_prepare_ragged writes what sd_verify_ragged then sd_pdraft_prepare_ragged write,
+    # byte for byte, and the oracle's ragged verify and rebuild
+    rng = np.random.default_rng(300 + B + K_max)
+    p, q, d, cu, T = ragged_case(rng, B, K_max, V, greedy_frac=greedy)
+    H, bs = 64, 16
+    pos0 = rng.integers(0, 2000, B).astype(np.int32)
+    width = (int(pos0.max()) + 2 * K_max) // bs + 1
+    table = rng.permutation(B * width).astype(np.int32).reshape(B, width)
+    hid = torch.from_numpy(rng.standard_normal((int(cu[-1]) + B, H)).astype(np.float32)).to(
+        torch.bfloat16).cuda()
+    hs = torch.from_numpy(rng.standard_normal(H).astype(np.float32)).to(torch.bfloat16).cuda()
+    Tt = to_dev(T) if temp else None
+    assert sd.sd_verify_prepare_kernels(B, K_max, V, sd.SD_F32_PROBS, temp) == kernels
+    cap = B * 2 * K_max
+
+    def outs():
+        fill = lambda shape, v, dt=torch.int32: torch.full(shape, v, dtype=dt, device="cuda")  # noqa
+        return dict(out_tokens=fill((B, K_max + 1), 77), num_accepted=fill((B,), 77),
+                    p_at=fill((B, K_max), 77.0, torch.float32),
+                    q_at=fill((B, K_max), 77.0, torch.float32),
+                    input_ids=fill((cap,), 77), positions=fill((cap,), 77),
+                    slot_mapping=fill((cap,), 77), hidden_map=fill((cap,), 77),
+                    is_masked=fill((cap,), 7, torch.uint8),
+                    is_rejected=fill((B, K_max + 1), 7, torch.uint8),
+                    start_loc=fill((B + 1,), 77), new_token_idx=fill((B, K_max), 77),
+                    total_out=fill((1,), 77),
+                    out_hidden=torch.zeros(cap, H, dtype=torch.bfloat16, device="cuda"),
+                    err=fill((1,), 0))
+
+    a, b = outs(), outs()
+    args = (to_dev(p), to_dev(q), to_dev(d), to_dev(cu))
+    sd.sd_verify_ragged(*args, a["out_tokens"], a["num_accepted"], temperature=Tt, seed=23,
+                        p_at_draft=a["p_at"], q_at_draft=a["q_at"], err=a["err"])
+    sd.sd_pdraft_prepare_ragged(a["out_tokens"], a["num_accepted"], args[3], _i32(pos0),
+                                _i32(table), bs, 10**6, a["input_ids"], a["positions"],
+                                a["slot_mapping"], a["hidden_map"], a["is_masked"],
+                                a["is_rejected"], a["start_loc"], a["new_token_idx"],
+                                a["total_out"], hid, hs, a["out_hidden"], err=a["err"])
+    ws = torch.zeros(sd.load().sd_verify_prepare_workspace_bytes(B), dtype=torch.uint8,
+                     device="cuda")
+    sd.sd_verify_prepare_ragged(*args, b["out_tokens"], b["num_accepted"], _i32(pos0),
+                                _i32(table), bs, 10**6, b["input_ids"], b["positions"],
+                                b["slot_mapping"], b["hidden_map"], b["is_masked"],
+                                b["is_rejected"], b["start_loc"], b["new_token_idx"],
+                                b["total_out"], hid, hs, b["out_hidden"], temperature=Tt,
+                                seed=23, p_at_draft=b["p_at"], q_at_draft=b["q_at"],
+                                err=b["err"], workspace_buf=ws)
+    torch.cuda.synchronize()
+    for k in a:
+        x, y = a[k], b[k]
+        if x.dtype == torch.bfloat16:
+            x, y = x.view(torch.int16), y.view(torch.int16)
+        assert torch.equal(x, y), k
+    assert int(ws.count_nonzero()) == 0 and int(b["err"].item()) == 0
+    ver = oracle.verify_ragged(p, q, d, cu, K_max, temperature=T if temp else None, seed=23)
+    assert np.array_equal(b["out_tokens"].cpu().numpy(), ver["out_tokens"])
+    want = oracle.pdraft_expand(ver["out_tokens"], ver["num_accepted"], pos0, table, bs, 10**6,
+                                cu=cu)
+    for k in KEYS:
+        assert np.array_equal(b[k].cpu().numpy().reshape(-1), want[k].reshape(-1)), k

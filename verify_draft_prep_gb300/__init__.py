@@ -35,7 +35,8 @@ EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
             "sd_verify_noalloc", "sd_draft_sample", "sd_pdraft_prepare_padded",
             "sd_verify_ragged", "sd_pdraft_prepare_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_race_E_check", "sd_status_string", "sd_version",
-            "sd_verify_prepare", "sd_verify_prepare_workspace_bytes", "sd_verify_prepare_kernels"]
+            "sd_verify_prepare", "sd_verify_prepare_workspace_bytes", "sd_verify_prepare_kernels",
+            "sd_verify_prepare_ragged"]
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +77,11 @@ def load():
                                           P, P, P, P, P, P, i32, P, i64, i32, P, P, i64, P,
                                           ctypes.c_size_t, P, P]
         lib.sd_verify_prepare.restype = i32
+        lib.sd_verify_prepare_ragged.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, P, u64,
+                                                 u32, P, P, P, P, P, P, i32, i32, ctypes.c_int32,
+                                                 i32, P, P, P, P, P, P, P, P, P, i32, P, i64, i32,
+                                                 P, P, i64, P, ctypes.c_size_t, P, P]
+        lib.sd_verify_prepare_ragged.restype = i32
         lib.sd_verify_prepare_workspace_bytes.argtypes = [i32]
         lib.sd_verify_prepare_workspace_bytes.restype = ctypes.c_size_t
         lib.sd_verify_prepare_kernels.argtypes = [i32, i32, i32, i32, i32]
@@ -242,6 +248,44 @@ def sd_verify_prepare(target, draft, drafts, out_tokens, num_accepted, pos0, blo
         _row_stride(target_hidden), target_hidden.shape[0], _ptr(h_shared), _ptr(out_hidden),
         _row_stride(out_hidden), _ptr(ws), ws.numel(), _ptr(err), _stream(target, stream))
     _check(rc, "sd_verify_prepare")
+
+
+def sd_verify_prepare_ragged(target, draft, drafts, cu_drafts, out_tokens, num_accepted, pos0,
+                             block_table, block_size, mask_token_id, input_ids, positions,
+                             slot_mapping, hidden_map, is_masked, is_rejected, start_loc,
+                             new_token_idx, total_out, target_hidden, h_shared, out_hidden,
+                             temperature=None, seed=0, p_at_draft=None, q_at_draft=None, err=None,
+                             stream=None, workspace_buf=None, request_base=0):
+    """sd_verify_ragged then sd_pdraft_prepare_ragged on its outputs, in one call (see
+    include/sd.h); shapes as for the two calls (out_tokens [B, K_max+1])."""
+    import torch
+
+    B, K1 = out_tokens.shape
+    V = target.shape[1]
+    if target.dtype == torch.float32:
+        dtype = SD_F32_PROBS
+    elif target.dtype == torch.bfloat16:
+        dtype = SD_BF16_LOGITS
+    else:
+        raise SDError("target must be float32 probabilities or bfloat16 logits")
+    if draft.dtype != target.dtype or cu_drafts.shape[0] != B + 1:
+        raise SDError("draft must match target; cu_drafts needs B+1 entries")
+    cap, H = out_hidden.shape
+    if input_ids.shape[0] != cap:
+        raise SDError("out_hidden must have one row per drafter slot")
+    ws = workspace_buf if workspace_buf is not None else workspace(_device(target), B, K1 - 1, V,
+                                                                   dtype)
+    rc = load().sd_verify_prepare_ragged(
+        B, K1 - 1, V, dtype, _ptr(target), _row_stride(target), _ptr(draft),
+        _row_stride(draft) if draft.shape[0] else V, _ptr(drafts), _ptr(cu_drafts),
+        _ptr(temperature), seed, request_base, _ptr(out_tokens), _ptr(num_accepted),
+        _ptr(p_at_draft), _ptr(q_at_draft), _ptr(pos0), _ptr(block_table), block_table.shape[1],
+        block_size, mask_token_id, cap, _ptr(input_ids), _ptr(positions), _ptr(slot_mapping),
+        _ptr(hidden_map), _ptr(is_masked), _ptr(is_rejected), _ptr(start_loc),
+        _ptr(new_token_idx), _ptr(total_out), H, _ptr(target_hidden),
+        _row_stride(target_hidden), target_hidden.shape[0], _ptr(h_shared), _ptr(out_hidden),
+        _row_stride(out_hidden), _ptr(ws), ws.numel(), _ptr(err), _stream(target, stream))
+    _check(rc, "sd_verify_prepare_ragged")
 
 
 def sd_verify_prepare_kernels(B, K, V, dtype, has_temperature):

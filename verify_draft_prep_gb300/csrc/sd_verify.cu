@@ -1184,23 +1184,25 @@ constexpr int kMaxFuseB = 192;
 // it, at the slot this CTA publishes in r's merge slot. The rebuild CTA of the last request also
 // writes total_out, start_loc[B] and the padding tail.
 __device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm) {
-  __shared__ int acc_s[kMaxFuseB];
+  __shared__ int acc_s[kMaxFuseB];  // a_q, then (after the scan) a_q + K_q
   const RebuildArgs& R = P.rb;
-  const int K = P.K, n = r + 1;
-  for (int q = threadIdx.x; q < n; q += NT) acc_s[q] = K;
+  const int KM = P.K, n = r + 1;  // K_max with per-request counts
+  for (int q = threadIdx.x; q < n; q += NT) acc_s[q] = req_rows(P, q).k;
   __syncthreads();
-  for (int p = threadIdx.x; p < n * K; p += NT) {
-    const int q = p / K, j = p - q * K;
+  for (int p = threadIdx.x; p < n * KM; p += NT) {
+    const int q = p / KM, j = p - q * KM;
+    const ReqRows rq = req_rows(P, q);
+    if (j >= rq.k) continue;
     float Pv, Qv;
     bool bad;
-    if (!draft_accepted(P, req_rows(P, q), q, j, Pv, Qv, bad)) atomicMin(&acc_s[q], j);
+    if (!draft_accepted(P, rq, q, j, Pv, Qv, bad)) atomicMin(&acc_s[q], j);
   }
   __syncthreads();
-  long long part = 0;
-  for (int q = threadIdx.x; q < r; q += NT) part += acc_s[q] + K;
-  const long long off = block_sum_ll(part, sm);
-  const int a = acc_s[r], L = a + K;
   const ReqRows rr = req_rows(P, r);
+  const int K = rr.k, a = acc_s[r], L = a + K;
+  long long part = 0;
+  for (int q = threadIdx.x; q < r; q += NT) part += acc_s[q] + req_rows(P, q).k;
+  const long long off = block_sum_ll(part, sm);
   int32_t e = 0;
   const int pos0 = __ldg(R.pos0 + r);
   const int32_t* bt_row = R.block_table + (size_t)r * R.max_blocks;
@@ -1217,8 +1219,8 @@ __device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm
                        R.slot_mapping, R.hidden_map, R.is_masked, e);
   }
   const int t = threadIdx.x;
-  if (t <= K) R.is_rejected[(size_t)r * (K + 1) + t] = (t >= 1 && t > a) ? 1 : 0;
-  if (t < K) R.new_token_idx[(size_t)r * K + t] = (int32_t)(off + a + t);
+  if (t <= KM) R.is_rejected[(size_t)r * (KM + 1) + t] = (t >= 1 && t > a && t <= K) ? 1 : 0;
+  if (t < KM) R.new_token_idx[(size_t)r * KM + t] = t < K ? (int32_t)(off + a + t) : -1;
   if (t == 0) {
     R.start_loc[r] = (int32_t)off;
     st_release_u32(&P.slots[r].off1, (unsigned)(off + 1));
@@ -1266,8 +1268,9 @@ __device__ __noinline__ void fused_finish(const VerifyParams& P, int r, int a, i
     if (v == 0u) {
       e |= SD_ERR_WAIT;
     } else {
+      // slot a_r exists when the request has drafter slots at all (K_r > 0: L_r = a_r + K_r)
       const long long g = (long long)v - 1 + a;
-      if (g < P.rb.capacity) P.rb.input_ids[g] = (int32_t)b;
+      if (req_rows(P, r).k > 0 && g < P.rb.capacity) P.rb.input_ids[g] = (int32_t)b;
       *slot = 0u;
     }
     raise_err(P.err, e);
@@ -1735,7 +1738,7 @@ struct VerifyShape {
   int cl, nc, race_blocks;
   bool fusable;
 };
-static VerifyShape verify_shape(int B, int V, int dtype, bool has_temperature, bool ragged) {
+static VerifyShape verify_shape(int B, int V, int dtype, bool has_temperature) {
   VerifyShape v;
   const int epu = dtype == SD_F32_PROBS ? 4 : 8;
   v.cl = choose_cluster(V, epu);
@@ -1754,7 +1757,7 @@ static VerifyShape verify_shape(int B, int V, int dtype, bool has_temperature, b
   // batch and at least as many racing (the race CTAs wait for the rebuild CTAs' published slots
   // only at their very end, and every CTA of the wave is resident from the start).
   v.fusable = v.race_blocks == 0 && v.cl == 1 && dtype == SD_F32_PROBS && !has_temperature &&
-              !ragged && B <= sdk::kMaxFuseB && 2L * B <= (long)sdk::kMinBlocksF32 * sm_count();
+              B <= sdk::kMaxFuseB && 2L * B <= (long)sdk::kMinBlocksF32 * sm_count();
   return v;
 }
 
@@ -1788,7 +1791,7 @@ static int verify_launch_impl(int B, int K, int V, int dtype, const void* target
   P.q_at = q_at_draft;
   P.slots = (sdk::RaceSlot*)workspace;
   P.err = err;
-  const VerifyShape shape = verify_shape(B, V, dtype, temperature != nullptr, cu_drafts != nullptr);
+  const VerifyShape shape = verify_shape(B, V, dtype, temperature != nullptr);
   P.cl = shape.cl;
   P.nc = shape.nc;
   P.race_blocks = shape.race_blocks;
@@ -1875,7 +1878,8 @@ extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int
 // rebuild CTA to the CTA that writes the final token).
 extern "C" int sd_verify_prepare_launch(
     int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
-    const int32_t* drafts, const float* temperature, uint64_t seed, uint32_t request_base,
+    const int32_t* drafts, const int32_t* cu_drafts, const float* temperature, uint64_t seed,
+    uint32_t request_base,
     int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
     const int32_t* pos0, const int32_t* block_table, int max_blocks, int block_size,
     int32_t mask_token_id, int capacity, int32_t* input_ids, int32_t* positions,
@@ -1910,11 +1914,11 @@ extern "C" int sd_verify_prepare_launch(
             ((uintptr_t)h_shared % 16 == 0) && ((uintptr_t)out_hidden % 16 == 0) &&
             (ld_in % 8 == 0) && (ld_out % 8 == 0);
   bool fused = false;
-  int rc = verify_launch_impl(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, nullptr,
+  int rc = verify_launch_impl(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts,
                               temperature, seed, request_base, out_tokens, num_accepted,
                               p_at_draft, q_at_draft, workspace, err, stream, &rb, &fused);
   if (rc != SD_OK || fused) return rc;
-  return sd_prep_launch(B, K, out_tokens, num_accepted, nullptr, pos0, block_table, max_blocks,
+  return sd_prep_launch(B, K, out_tokens, num_accepted, cu_drafts, pos0, block_table, max_blocks,
                         block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
                         hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out,
                         H, target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
@@ -1926,7 +1930,7 @@ extern "C" int sd_verify_prepare_kernel_count(int B, int K, int V, int dtype,
                                               int has_temperature) {
   (void)K;
   if (B == 0) return 0;
-  return verify_shape(B, V, dtype, has_temperature != 0, false).fusable ? 1 : 2;
+  return verify_shape(B, V, dtype, has_temperature != 0).fusable ? 1 : 2;
 }
 
 // ------------------------------------------------------------------ no-allocation entry point
