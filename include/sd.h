@@ -275,8 +275,10 @@ SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int3
  * The two operations are those of sd_verify (speculative-decoding explainer, sections "核心思想"
  * and "修正拒绝采样") and sd_pdraft_prepare (P-EAGLE blog, sections "Triton Kernel" and "Hidden
  * State 管理"), with sd_verify's out_tokens and num_accepted feeding the rebuild. When every
- * request samples (temperature NULL) on probability rows and the batch fits one wave of CTAs,
- * both run in a single launch: B extra CTAs rebuild the drafter batch while the others race.
+ * request samples (temperature NULL) on probability rows, the batch is small enough for one
+ * wave of CTAs (B <= 192, and 2B no more than 5 CTAs per SM) and sd_verify would split each row
+ * over a request's CTAs (rather than its large-batch race kernel), both run in a single launch:
+ * B extra CTAs rebuild the drafter batch while the others race.
  * A rebuild CTA recomputes the accept decisions of its request and of those before it (they
  * depend on the inputs only), takes its first drafter slot as their prefix, and writes its
  * request's rows and hidden states; only the final token at slot a_r waits for the race, and the
@@ -290,7 +292,7 @@ SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int3
  * and num_accepted are this call's own outputs), with one workspace of at least
  * sd_verify_prepare_workspace_bytes(B) bytes (as much as sd_verify's), 16-byte aligned, zeroed
  * before first use and left zeroed by every call. Errors: those of both calls; SD_ERR_WAIT if a
- * request's published slot never appeared (its final token is then not written).
+ * request's published slot never appeared (its final token is then not written to input_ids).
  */
 SD_API int sd_verify_prepare(
     int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
