@@ -116,3 +116,14 @@ def test_verify_prepare_host_checks(lib):
     assert lib.sd_verify_prepare_kernels(4, 2, 10, 7, 0) == -3
     assert lib.sd_verify_prepare_kernels(4, 0, 10, 0, 0) == -2
     assert lib.sd_verify_prepare_kernels(0, 2, 10, 0, 0) == 0
+
+
+def test_error_bits_match_the_header():
+    # every SD_ERR_* bit of include/sd.h has the same value in the Python package, and no two
+    # bits share a value
+    text = open(os.path.join(ROOT, "include", "sd.h")).read()
+    bits = dict((n, int(v)) for n, v in re.findall(r"#define (SD_ERR_\w+) (\d+)", text))
+    assert bits and len(set(bits.values())) == len(bits)
+    for name, value in bits.items():
+        assert getattr(sd, name) == value, name
+        assert value & (value - 1) == 0, name  # a single bit
