@@ -127,3 +127,14 @@ def test_error_bits_match_the_header():
     for name, value in bits.items():
         assert getattr(sd, name) == value, name
         assert value & (value - 1) == 0, name  # a single bit
+
+
+def test_constants_match_the_header():
+    text = open(os.path.join(ROOT, "include", "sd.h")).read()
+    for name in ("SD_F32_PROBS", "SD_BF16_LOGITS", "SD_K_MAX", "SD_VERIFY_NOALLOC_MAX_B"):
+        m = re.search(r"#define %s (\d+)" % name, text)
+        assert m and getattr(sd, name) == int(m.group(1)), name
+    # every status code has its own text
+    codes = [int(v) for v in re.findall(r"#define SD_E_\w+ \((-\d+)\)", text)]
+    texts = {sd.load().sd_status_string(c) for c in codes + [0]}
+    assert len(texts) == len(codes) + 1
