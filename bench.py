@@ -6,10 +6,12 @@ resident in HBM. W warm-up steps, then exactly K timed steps replayed from CUDA 
 over several input sets (whose rows together exceed the 129 MB L2). Prints one JSON line
 (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config b64] [--impl gb300|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config b1024lg] [--impl gb300|reference]
 
---impl reference times the plain CPU oracle (the baseline this library is checked against) on
-the host cores for the same workload and metric.
+The timed workload is b1024lg (B=1024, K=8, V=201088 bf16 logits, the largest configuration);
+b64, b256mix and b512rag are then timed the same way in the same process and reported under
+"configs". --impl reference times the plain CPU oracle (the baseline this library is checked
+against) on the host cores for the same workload, inputs and metric.
 """
 
 from __future__ import annotations
@@ -151,13 +153,13 @@ def algorithmic_bytes(w, a):
     return verify, expand, gather, verify_read
 
 
-def make_sets(cfg_name, nsets, device, rank, batch=None):
+def make_set(cfg_name, s, device, rank, batch=None):
+    """Input set s of a workload on this rank (set 0 is also what the oracle baselines time)."""
     import workloads
 
     idx = [c["name"] for c in workloads.CONFIGS].index(cfg_name)
-    return [workloads.make(idx, device=device, gen_seed=1000 + idx + 101 * s + 7919 * rank,
-                           B=batch)
-            for s in range(nsets)]
+    return workloads.make(idx, device=device, gen_seed=1000 + idx + 101 * s + 7919 * rank,
+                          B=batch)
 
 
 def alloc_outputs(w, device):
@@ -257,32 +259,74 @@ def time_graph(fn, sets, outs, stream, K):
     return a.elapsed_time(b) / K
 
 
-def run_cpu_baseline(w_host, budget_s=10.0):
-    """Time the oracle (as it stands) on all host cores on one input set: requests/s."""
+def oracle_pass(hc, nthreads):
+    """One pass of the oracle over every request of the host copy hc: verify, expand, gather."""
     import oracle
 
-    cores = len(os.sched_getaffinity(0))
-    B, K, V = w_host["B"], w_host["K"], w_host["V"]
-    reps, t0 = 0, time.perf_counter()
+    if hc["kind"] == "probs":
+        res = oracle.verify_probs(hc["target"], hc["draft"], hc["drafts"],
+                                  temperature=hc["temperature"], seed=0, nthreads=nthreads)
+    else:
+        res = oracle.verify_logits(hc["target"], hc["draft"], hc["drafts"],
+                                   temperature=hc["temperature"], seed=0, nthreads=nthreads,
+                                   margins=False)
+    e = oracle.pdraft_expand(res["out_tokens"], res["num_accepted"], hc["pos0"],
+                             hc["block_table"], hc["block_size"], hc["mask"])
+    oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], hc["hidden"], hc["h_shared"])
+
+
+def first_requests(hc, n):
+    """The first n requests of a host copy (a bounded sample of the batch)."""
+    K = hc["K"]
+    out = dict(hc)
+    for k in ("target", "draft", "drafts", "temperature", "pos0", "block_table"):
+        out[k] = hc[k][:n]
+    out["hidden"] = hc["hidden"][:n * (K + 1)]
+    out["B"] = n
+    return out
+
+
+def oracle_rate(hc, nthreads, budget_s, max_passes=100000):
+    """Requests/s of the oracle (as it stands) on hc: whole passes until budget_s has elapsed."""
+    passes, t0 = 0, time.perf_counter()
     while True:
-        if w_host["kind"] == "probs":
-            res = oracle.verify_probs(w_host["target"], w_host["draft"], w_host["drafts"],
-                                      temperature=w_host["temperature"], seed=0, nthreads=cores)
-        else:
-            res = oracle.verify_logits(w_host["target"], w_host["draft"], w_host["drafts"],
-                                       temperature=w_host["temperature"], seed=0,
-                                       nthreads=cores, margins=False)
-        e = oracle.pdraft_expand(res["out_tokens"], res["num_accepted"], w_host["pos0"],
-                                 w_host["block_table"], w_host["block_size"], w_host["mask"])
-        oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], w_host["hidden"],
-                             w_host["h_shared"])
-        reps += 1
+        oracle_pass(hc, nthreads)
+        passes += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 5000:
-            break
-    return {"value": B * reps / el, "unit": "requests/s", "cores": cores, "kind": "oracle",
-            "sample": f"{reps} passes over all {B} requests of one input set "
-                      f"(verify + expand + gather), {el:.1f} s"}
+        if el >= budget_s or passes >= max_passes:
+            return hc["B"] * passes / el, passes, el
+
+
+def sized_sample(hc, nthreads, seconds):
+    """The largest prefix of the batch whose oracle pass takes about `seconds` (measured on a
+    probe of a few requests per thread), at least one request."""
+    n = min(hc["B"], max(1, 2 * max(1, nthreads)))
+    probe = first_requests(hc, n)
+    t0 = time.perf_counter()
+    oracle_pass(probe, nthreads)
+    per_pass = time.perf_counter() - t0
+    # requests are spread over the threads: a pass of m requests takes ~ceil(m/threads) rounds
+    per_round = per_pass / max(1, -(-n // max(1, nthreads)))
+    m = int(seconds / max(per_round, 1e-9)) * max(1, nthreads)
+    return first_requests(hc, max(1, min(hc["B"], m)))
+
+
+def run_cpu_baseline(hc, budget_s=10.0, single_s=4.0):
+    """The oracle (as it stands) on this process's host cores, on the same inputs as the GPU
+    (set 0 of the timed workload): all cores over whole passes of the batch, then one thread on
+    a bounded prefix of it."""
+    cores = len(os.sched_getaffinity(0))
+    sample = sized_sample(hc, cores, budget_s / 2) if hc["B"] > 1 else hc
+    v, passes, el = oracle_rate(sample, cores, budget_s)
+    one = sized_sample(hc, 1, single_s / 2)
+    v1, passes1, el1 = oracle_rate(one, 1, single_s)
+    return {"value": v, "unit": "requests/s", "cores": cores, "kind": "oracle",
+            "sample": f"{passes} passes over the first {sample['B']} of the batch's {hc['B']} "
+                      f"requests (set 0 of the timed inputs; verify + expand + gather) on "
+                      f"{cores} threads, {el:.1f} s",
+            "single_thread": {"value": v1, "unit": "requests/s", "cores": 1,
+                              "sample": f"{passes1} passes over the first {one['B']} requests on "
+                                        f"one thread, {el1:.1f} s"}}
 
 
 def host_copy(w):
@@ -303,54 +347,43 @@ def host_copy(w):
                 h_shared=bits(w.h_shared))
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="b64")
-    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: auto)")
-    ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=0,
-                    help="profiling aid: the config's shapes with this many requests (0: as "
-                         "configured); a line with a reduced batch is not the config's number")
-    ap.add_argument("--step-events", action="store_true",
-                    help="record an event at every step boundary (per-step times; the event "
-                         "nodes break the programmatic launch edge between steps)")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+# The configurations measured besides the timed one (every configuration of the bar on one
+# record); the launch-bound one-request case is a parity case only.
+EXTRA_CONFIGS = ("b64", "b256mix", "b512rag")
 
+
+def config_dict(cfg, B, nsets, rows_gb, world, batch):
+    import workloads
+
+    return {"workload": workloads.config_label(cfg) + (
+                f" [reduced to B={B} for profiling]" if batch else ""),
+            "B": B, "K": cfg["K"], "V": cfg["V"], "H": cfg["H"],
+            "l2": f"{nsets} rotating input sets (rows of all sets {rows_gb:.1f} GB > 129 MB L2; "
+                  f"a set recurs after {nsets - 1} others)",
+            "timing": "CUDA graphs of the timed steps, one sd_verify_prepare call each (one "
+                      "launch when the batch is all-sampled and fits one wave, else verify then "
+                      "the rebuild as its programmatic dependent); the dominant kernel alone in "
+                      "a second graph for the roofline",
+            "parallelism": f"dp{world}: request shards of {B} per GPU"}
+
+
+def n_sets(cfg):
+    return 4 if cfg["B"] * cfg["V"] < 64 * 201088 * 2 else 2
+
+
+def measure(name, args, sd, device, rank, world, steps, keep_set0=False):
+    """Time `steps` steps of one workload (W warm-up steps first) and its kernels; returns the
+    figures (and set 0 when keep_set0, for the end-to-end and oracle legs)."""
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
-
-    if args.impl == "reference":
-        if rank == 0:
-            run_reference(args, world)
-        if world > 1:
-            dist.destroy_process_group()
-        return
-
-    torch.cuda.set_device(local)
-    device = f"cuda:{local}"
-    import verify_draft_prep_gb300 as sd
-
-    sd.load()
     import workloads
     from verify_draft_prep_gb300 import shard
 
-    cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
+    cfg = [c for c in workloads.CONFIGS if c["name"] == name][0]
     batch = args.batch or None
-    w0 = workloads.make(args.config, device=device, gen_seed=1000 + 7919 * rank, B=batch)
-    nsets = args.sets or (4 if cfg["B"] * cfg["V"] < 64 * 201088 * 2 else 2)
-    sets = [w0] + make_sets(args.config, nsets - 1, device, rank + 1, batch)
+    nsets = args.sets or n_sets(cfg)
+    sets = [make_set(name, s, device, rank, batch) for s in range(nsets)]
     outs = [alloc_outputs(w, device) for w in sets]
     for w in sets:
         temperatures(w)  # decided before any graph capture (it reads the device)
@@ -358,7 +391,6 @@ def main():
         # the Philox counters (weak scaling, no exchange on the data path)
         w.request_base = shard.request_base(w.B)[0] if world > 1 else 0
 
-    # warm-up (untimed), then algorithmic bytes from each set's accepted counts
     stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -368,7 +400,7 @@ def main():
     # the timed steps are replayed from CUDA graphs of up to CHUNK steps (a graph of K % CHUNK
     # steps makes up the rest, so exactly K steps run); the timed region is bracketed by two
     # events (per-step events only with --step-events)
-    K = args.steps
+    K = steps
     CHUNK = min(K, 200)
 
     def capture(n, with_events):
@@ -396,7 +428,7 @@ def main():
     full, rest = divmod(K, CHUNK)
     graph_rest = capture(rest, False)[0] if rest else None
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(int(str(device).split(":")[-1]))
     clocks.start()
     time.sleep(0.3)
     if world > 1:
@@ -423,8 +455,8 @@ def main():
         per_set.append(algorithmic_bytes(w, a)[:3] + (a, algorithmic_bytes(w, a)[3]))
     errs = [int(o["err"].item()) for o in outs]
     step_ms = [evs[s].elapsed_time(evs[s + 1]) for s in range(CHUNK)] if evs else []
-    # the dominant kernel alone, K launches in a graph of its own, right after the timed region:
-    # the fused step kernel when the step is one launch, else the verify kernel
+    # the dominant kernel alone, CHUNK launches in a graph of its own, right after the timed
+    # region: the fused step kernel when the step is one launch, else the verify kernel
     dt_code = 0 if cfg["kind"] == "probs" else 1
     has_t = temperatures(sets[0]) is not None
     step_kernels = sd.sd_verify_prepare_kernels(sets[0].B, sets[0].K, sets[0].V, dt_code, has_t)
@@ -457,81 +489,164 @@ def main():
     avg_dom = avg_f if fused else avg_v
     achieved = bytes_dom / (avg_dom * 1e-3) / 1e9
     traffic, traffic_note = (None, "no capture of the current kernel source")
-    if not args.batch and (args.config, _src_hash()) in MEASURED_TRAFFIC:
-        traffic, traffic_note = MEASURED_TRAFFIC[(args.config, _src_hash())]
-
-    # end to end through the public API: pinned host inputs -> device, step, results -> host
-    e2e = run_e2e(sd, sets[0], device, args.e2e_steps)
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = run_cpu_baseline(host_copy(sets[0]))
-
-    # kernels per step: one fused launch, or the verify kernel and the rebuild kernel
-    launches = step_kernels
+    if not args.batch and (name, _src_hash()) in MEASURED_TRAFFIC:
+        traffic, traffic_note = MEASURED_TRAFFIC[(name, _src_hash())]
     a_all = np.concatenate([p[3] for p in per_set])
     w0s = sets[0]
     sample_bytes = w0s.B * w0s.K * w0s.V * w0s.draft.element_size() + w0s.B * w0s.K * 4 + w0s.B * 4
     pad_bytes = float(np.mean([
         int(((per_set[s % nsets][3] + 1) * 2 * w0s.H).sum()) + w0s.B * 2 * w0s.K * (2 * w0s.H + 18)
         + w0s.B * (w0s.K + 1) * 4 + w0s.B * w0s.K * 4 for s in range(CHUNK)]))
-    prepare_padded = {"kernel": "sd_pdraft_prepare_padded", "us": avg_pp * 1e3,
-                      "bytes_per_launch": pad_bytes,
-                      "achieved_GBps": pad_bytes / (avg_pp * 1e-3) / 1e9,
-                      "frac": pad_bytes / (avg_pp * 1e-3) / 1e9 / peak,
-                      "rows": f"B*2K = {w0s.B * 2 * w0s.K} drafter rows, every one written "
-                              "(hidden states read for the a_r + 1 target rows of each request)"}
-    draft_sample = {"kernel": "sd_draft_sample", "us": avg_s * 1e3, "bytes_per_launch": sample_bytes,
-                    "achieved_GBps": sample_bytes / (avg_s * 1e-3) / 1e9,
-                    "frac": sample_bytes / (avg_s * 1e-3) / 1e9 / peak,
-                    "rows": f"B*K = {w0s.B * w0s.K} rows of V = {w0s.V}, each read once from HBM "
-                            "(logit rows: softmax statistics, then the race, the second pass "
-                            "mostly from L2)"}
-    info = {
-        "verify_ms": avg_v, "prepare_ms": avg_p,
-        "step_ms_median": float(np.median(step_ms)) if step_ms else None,
-        "step_bytes": bytes_all,
-        "step_GBps": bytes_all / (ms_per_step * 1e-3) / 1e9,
-        "mean_accepted": float(a_all.mean()), "err": errs,
+    rows_gb = nsets * w0s.target.numel() * w0s.target.element_size() / 1e9
+    logits = cfg["kind"] != "probs"
+    roofline = {
+        "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_note,
+        "kernel": "sd_verify_prepare (verify and rebuild in one launch)" if fused else "sd_verify",
+        "kernel_us": avg_dom * 1e3, "peak_source": peak_kind,
+        "algorithmic_bytes_per_launch": bytes_dom,
+        "bytes_model": ("minimum bytes (scalar gathers + one p and one q row per sampled request, "
+                        "a_r + 1 rows per greedy one)" if not logits else
+                        "full rows (2K + 1 logit rows per request)")
+        + ("; plus the rebuild's slots and hidden rows" if fused else ""),
+        "verify_alone": {"us": avg_v * 1e3, "bytes": bytes_v,
+                         "frac": bytes_v / (avg_v * 1e-3) / 1e9 / peak},
+        # the verify kernel against the bytes it must read (rows up to the first rejection):
+        # its own efficiency, whatever the roofline model of the variant
+        "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
+        "rows_read_bytes": bytes_read,
+        "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak,
     }
-    print(json.dumps({"info": info}), file=sys.stderr)
+    res = {
+        "cfg": cfg, "B": B, "steps": K, "value": value, "ms_per_step": ms_per_step,
+        "launches": step_kernels, "clocks": clk, "roofline": roofline,
+        "config": config_dict(cfg, B, nsets, rows_gb, world, batch),
+        "dtype": "f32" if not logits else "bf16",
+        "draft_sample": {"kernel": "sd_draft_sample", "us": avg_s * 1e3,
+                         "bytes_per_launch": sample_bytes,
+                         "achieved_GBps": sample_bytes / (avg_s * 1e-3) / 1e9,
+                         "frac": sample_bytes / (avg_s * 1e-3) / 1e9 / peak,
+                         "rows": f"B*K = {w0s.B * w0s.K} rows of V = {w0s.V}, each read once "
+                                 "from HBM"},
+        "prepare_padded": {"kernel": "sd_pdraft_prepare_padded", "us": avg_pp * 1e3,
+                           "bytes_per_launch": pad_bytes,
+                           "achieved_GBps": pad_bytes / (avg_pp * 1e-3) / 1e9,
+                           "frac": pad_bytes / (avg_pp * 1e-3) / 1e9 / peak,
+                           "rows": f"B*2K = {w0s.B * 2 * w0s.K} drafter rows, every one written "
+                                   "(hidden states read for the a_r + 1 target rows of each "
+                                   "request)"},
+        "info": {"verify_ms": avg_v, "prepare_ms": avg_p,
+                 "step_ms_median": float(np.median(step_ms)) if step_ms else None,
+                 "step_bytes": bytes_all,
+                 "step_GBps": bytes_all / (ms_per_step * 1e-3) / 1e9,
+                 "mean_accepted": float(a_all.mean()), "err": errs},
+    }
+    if keep_set0:
+        res["set0"] = sets[0]
+    del sets, outs, graph, graph_rest
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def summary(r, cpu=None):
+    """The figures of one configuration in the record's per-configuration table."""
+    rf = r["roofline"]
+    out = {"workload": r["config"]["workload"], "value": r["value"], "unit": "requests/s",
+           "ms_per_step": r["ms_per_step"], "steps": r["steps"],
+           "gpu_launches": r["launches"] * r["steps"],
+           "kernel": rf["kernel"], "kernel_us": rf["kernel_us"], "frac": rf["frac"],
+           "frac_rows_read": rf["frac_rows_read"], "step_frac": rf["step_frac"],
+           "verify_alone": rf["verify_alone"], "traffic": rf["traffic"],
+           "algorithmic_bytes_per_launch": rf["algorithmic_bytes_per_launch"],
+           "bytes_model": rf["bytes_model"], "clocks": r["clocks"],
+           "mean_accepted": r["info"]["mean_accepted"], "err": r["info"]["err"],
+           "draft_sample": r["draft_sample"], "prepare_padded": r["prepare_padded"]}
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="b1024lg")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0: auto)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --config (not the other configurations)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: the config's shapes with this many requests (0: as "
+                         "configured); a line with a reduced batch is not the config's number")
+    ap.add_argument("--step-events", action="store_true",
+                    help="record an event at every step boundary (per-step times; the event "
+                         "nodes break the programmatic launch edge between steps)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    import verify_draft_prep_gb300 as sd
+
+    sd.load()
+
+    main_res = measure(args.config, args, sd, device, rank, world, args.steps, keep_set0=True)
+    w0 = main_res.pop("set0")
+    # end to end through the public API: pinned host inputs -> device, step, results -> host
+    e2e = run_e2e(sd, w0, device, args.e2e_steps)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(host_copy(w0))
+    del w0
+    torch.cuda.empty_cache()
+
+    # the other configurations of the bar, each timed the same way in this process
+    extras = {}
+    if not args.no_extra and not args.batch:
+        for name in EXTRA_CONFIGS:
+            if name == args.config:
+                continue
+            r = measure(name, args, sd, device, rank, world, args.steps, keep_set0=rank == 0
+                        and not args.no_cpu_baseline)
+            c = None
+            if "set0" in r:
+                c = run_cpu_baseline(host_copy(r.pop("set0")), budget_s=3.0, single_s=1.5)
+                torch.cuda.empty_cache()
+            extras[name] = summary(r, c)
+
+    print(json.dumps({"info": main_res["info"]}), file=sys.stderr)
     if rank == 0:
+        K = args.steps
         line = {
-            "metric": METRIC, "value": value, "unit": "requests/s", "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32"
-            if cfg["kind"] == "probs" else "bf16", "data": "synthetic",
-            "config": {"workload": workloads.config_label(cfg) + (
-                f" [reduced to B={B} for profiling]" if args.batch else ""), "B": B,
-                       "K": sets[0].K,
-                       "V": sets[0].V, "H": sets[0].H,
-                       "l2": f"{nsets} rotating input sets (rows of all sets "
-                             f"{nsets * sets[0].target.numel() * sets[0].target.element_size() / 1e9:.1f} GB"
-                             f" > 129 MB L2; a set recurs after {nsets - 1} others)",
-                       "timing": "CUDA graphs of the timed steps, one sd_verify_prepare call "
-                                 "each (one launch when the batch is all-sampled and fits one "
-                                 "wave, else verify then the rebuild as its programmatic "
-                                 "dependent); the dominant kernel alone in a second graph for "
-                                 "the roofline",
-                       "parallelism": f"dp{world}: request shards of {B} per GPU"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "traffic_source": traffic_note,
-                         "kernel": "sd_verify_prepare (verify and rebuild in one launch)"
-                         if fused else "sd_verify", "kernel_us": avg_dom * 1e3,
-                         "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": bytes_dom,
-                         "bytes_model": ("minimum bytes (scalar gathers + one p and one q row "
-                                         "per sampled request, a_r + 1 rows per greedy one)"
-                                         if cfg["kind"] == "probs" else
-                                         "full rows (2K + 1 logit rows per request)")
-                         + ("; plus the rebuild's slots and hidden rows" if fused else ""),
-                         "verify_alone": {"us": avg_v * 1e3, "bytes": bytes_v,
-                                          "frac": bytes_v / (avg_v * 1e-3) / 1e9 / peak},
-                         "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
-                         "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches * K, "clocks": clk,
-            "draft_sample": draft_sample, "prepare_padded": prepare_padded,
+            "metric": METRIC, "value": main_res["value"], "unit": "requests/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": main_res["dtype"], "data": "synthetic", "config": main_res["config"],
+            "roofline": main_res["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": main_res["launches"] * K, "clocks": main_res["clocks"],
+            "draft_sample": main_res["draft_sample"],
+            "prepare_padded": main_res["prepare_padded"],
+            "configs": extras,
         }
         print(json.dumps(line))
     if world > 1:
@@ -660,55 +775,29 @@ def run_e2e(sd, w, device, steps):
 
 
 def run_reference(args, world):
-    """The oracle on the host cores, same workload, metric and unit."""
-    import torch  # noqa: F401
+    """The oracle on the host cores: the same workload, inputs (set 0 of the timed workload, made
+    by the same generator on the GPU when there is one), metric and unit as the timed arm. Each
+    step is one oracle pass over a bounded prefix of the batch, sized so that the warm-up and
+    timed steps take about two minutes at most."""
+    import torch
 
     import workloads
 
     cfg = [c for c in workloads.CONFIGS if c["name"] == args.config][0]
-    w = workloads.make(args.config, device="cpu")
+    device = "cuda:0" if torch.cuda.is_available() else "cpu"
+    w = make_set(args.config, 0, device, 0, args.batch or None)
     hc = host_copy(w)
-    import oracle
-
+    B, nsets = w.B, args.sets or n_sets(cfg)
+    rows_gb = nsets * w.target.numel() * w.target.element_size() / 1e9
+    del w
     cores = len(os.sched_getaffinity(0))
-    full_B = w.B
-
-    def sample(n):  # the first n requests of the batch
-        out = dict(hc)
-        for k in ("target", "draft", "drafts", "temperature", "pos0", "block_table"):
-            out[k] = hc[k][:n]
-        out["hidden"] = hc["hidden"][:n * (w.K + 1)]
-        return out
-
-    def step():
-        if hc["kind"] == "probs":
-            res = oracle.verify_probs(hc["target"], hc["draft"], hc["drafts"],
-                                      temperature=hc["temperature"], seed=0, nthreads=cores)
-        else:
-            res = oracle.verify_logits(hc["target"], hc["draft"], hc["drafts"],
-                                       temperature=hc["temperature"], seed=0, nthreads=cores,
-                                       margins=False)
-        e = oracle.pdraft_expand(res["out_tokens"], res["num_accepted"], hc["pos0"],
-                                 hc["block_table"], hc["block_size"], hc["mask"])
-        oracle.hidden_gather(int(e["total_out"][0]), e["hidden_map"], hc["hidden"],
-                             hc["h_shared"])
-
-    # each step is a bounded sample of the batch (its first Bs requests), sized so that the
-    # warm-up and timed steps together take about two minutes at most
-    probe_n = min(full_B, 8)
-    full = hc
-    hc = sample(probe_n)
-    t0 = time.perf_counter()
-    step()
-    per_req = (time.perf_counter() - t0) / probe_n
-    Bs = int(max(1, min(full_B, 120.0 / max(1e-9, per_req * (args.steps + args.warmup)))))
-    hc = sample(Bs) if Bs != probe_n else hc
-    del full
+    hs = sized_sample(hc, cores, 100.0 / max(1, args.steps + args.warmup))
+    Bs = hs["B"]
     for _ in range(args.warmup):
-        step()
+        oracle_pass(hs, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        oracle_pass(hs, cores)
     el = time.perf_counter() - t0
     value = Bs * args.steps / el
     line = {
@@ -716,11 +805,11 @@ def run_reference(args, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if cfg["kind"] == "probs" else "bf16",
-        "data": "synthetic", "config": {"workload": workloads.config_label(cfg), "B": w.B,
-                                        "K": w.K, "V": w.V, "H": w.H},
+        "data": "synthetic", "config": config_dict(cfg, B, nsets, rows_gb, world, args.batch),
         "cpu_baseline": {"value": value, "unit": "requests/s", "cores": cores, "kind": "oracle",
                          "sample": f"every step verifies and rebuilds the first {Bs} of the "
-                                   f"batch's {full_B} requests"},
+                                   f"batch's {B} requests (set 0 of the timed inputs) on "
+                                   f"{cores} threads"},
         "e2e": {"value": value, "unit": "requests/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -53,3 +53,36 @@ def test_traffic_table_names_known_configs():
     names = {c["name"] for c in workloads.CONFIGS}
     for (cfg, h), (bytes_, note) in bench.MEASURED_TRAFFIC.items():
         assert cfg in names and len(h) == 16 and bytes_ > 0 and "ncu" in note
+
+
+def test_oracle_samples_hold_the_requests_they_count():
+    # a timed oracle pass over a prefix of the batch must verify exactly the requests it counts
+    w = workloads.make("small", device="cpu", B=12)
+    hc = bench.host_copy(w)
+    s = bench.first_requests(hc, 5)
+    assert s["B"] == 5
+    for k in ("target", "draft", "drafts", "temperature", "pos0", "block_table"):
+        assert s[k].shape[0] == 5, k
+    assert s["hidden"].shape[0] == 5 * (w.K + 1)
+    # a prefix of a prefix is taken from the whole batch's arrays, not a stale sample
+    s2 = bench.first_requests(hc, 9)
+    assert s2["target"].shape[0] == 9 and np.array_equal(s2["target"][:5], s["target"])
+    v, passes, el = bench.oracle_rate(s, 1, 0.01)
+    assert passes >= 1 and abs(v - 5 * passes / el) <= 1e-9 * v
+    sz = bench.sized_sample(hc, 2, 0.05)
+    assert 1 <= sz["B"] <= 12 and sz["target"].shape[0] == sz["B"]
+
+
+def test_reference_arm_prints_the_timed_arms_config(capsys):
+    import argparse
+    import json
+
+    args = argparse.Namespace(config="small", steps=2, warmup=1, sets=0, batch=0)
+    bench.run_reference(args, 1)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    cfg = [c for c in workloads.CONFIGS if c["name"] == "small"][0]
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "requests/s"
+    assert line["config"]["workload"] == bench.config_dict(cfg, 1, 4, 0.0, 1, 0)["workload"]
+    assert set(line["config"]) == set(bench.config_dict(cfg, 1, 4, 0.0, 1, 0))
+    assert line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
