@@ -20,8 +20,10 @@
  *     pointer, bad size, misaligned pointer, launch failure). Nothing is enqueued on error.
  *   - Data errors found on the device (a draft token outside [0, V), a position the block table
  *     does not cover, ...) are OR-ed as SD_ERR_* bits into *err (a device int32 the caller
- *     zeroes; may be NULL). The kernel then takes the documented fallback. No kernel traps,
- *     asserts or waits on a flag.
+ *     zeroes; may be NULL). The kernel then takes the documented fallback. No kernel traps or
+ *     asserts. One kernel waits on a value written by another CTA of the same launch: the
+ *     single launch of sd_verify_prepare (see there), whose wait is bounded by time (20 ms on
+ *     the GPU clock) and ends with SD_ERR_WAIT, never with a hang.
  *
  * Notation: B requests, K drafts per request (1 <= K <= SD_K_MAX), V vocabulary entries,
  * H hidden size. Target rows p_0..p_K of request r are rows r*(K+1)+j of `target`; draft rows
@@ -63,8 +65,8 @@ extern "C" {
 #define SD_ERR_ZERO_ROW 16      /* a race row without a positive key even on p: token 0 */
 #define SD_ERR_TOTAL_RANGE 32   /* total_out outside [0, capacity]: clamped */
 #define SD_ERR_WAIT 64          /* sd_verify_prepare: a request's first drafter slot was not
-                                   published within the bounded wait; its final token is not
-                                   written to input_ids */
+                                   published within the bounded wait (20 ms); its final token is
+                                   not written to input_ids */
 #define SD_ERR_DRAFT_COUNT 128  /* cu_drafts gives a request a draft count outside [0, K_max]:
                                    clamped (sd_verify_ragged) */
 
@@ -176,8 +178,9 @@ SD_API int sd_verify_kernels(int B, int V, int dtype, int has_temperature);
  *   - B > SD_VERIFY_NOALLOC_MAX_B returns SD_E_NOALLOC_LIMIT and enqueues nothing.
  *   - The first call on a device looks the array's address up (cudaGetSymbolAddress) with that
  *     device current; make that first call before any stream capture.
- *   - Each call enqueues a clear of the slots it uses and then the verify kernel; it calls no
- *     allocator.
+ *   - Each call enqueues a clear of the slots it uses (one cudaMemsetAsync of B*16 bytes) and
+ *     then the verify kernel: two stream operations, of which sd_verify_kernels counts only the
+ *     kernel. It calls no allocator.
  *   - All calls on a device share the one array: calls that may overlap on the GPU (other
  *     streams, other host threads) race on it and must be serialised by the caller.
  */
@@ -278,15 +281,21 @@ SD_API int sd_pdraft_prepare(int B, int K, const int32_t* out_tokens, const int3
  * request samples (temperature NULL) on probability rows, the batch is small enough for one
  * wave of CTAs (B <= 192, and 2B no more than 5 CTAs per SM) and sd_verify would split each row
  * over a request's CTAs (rather than its large-batch race kernel), both run in a single launch:
- * B extra CTAs rebuild the drafter batch while the others race.
+ * B extra CTAs rebuild the drafter batch while the others race. The single launch is taken
+ * only when every one of its CTAs fits on the device at once (the occupancy API's count of
+ * resident CTAs per SM times the SMs).
  * A rebuild CTA recomputes the accept decisions of its request and of those before it (they
  * depend on the inputs only), takes its first drafter slot as their prefix, and writes its
  * request's rows and hidden states; only the final token at slot a_r waits for the race, and the
  * CTA that completes request r's race row writes it at the slot the rebuild CTA published in the
- * workspace (a bounded wait, never taken in practice: the slot appears microseconds after the
- * launch starts, the race rows complete tens of microseconds later). Other batches run the two
- * kernels back to back. Either way every output is bit for bit what sd_verify then
- * sd_pdraft_prepare write.
+ * workspace. If that CTA finds nothing published, it polls for at most 20 ms of the GPU clock
+ * (in practice it never waits: the slot appears microseconds after the launch starts, the race
+ * rows complete tens of microseconds later; a rebuild CTA kept off the GPU, for instance by
+ * other work on another stream filling the SMs, is the only way to run the wait out). When the
+ * wait runs out, SD_ERR_WAIT is raised and that request's final token is not written to
+ * input_ids (every other output is); the two CTAs still leave the workspace zeroed. Other
+ * batches run the two kernels back to back. Either way every output is bit for bit what
+ * sd_verify then sd_pdraft_prepare write.
  *
  * Arguments: sd_verify's (without cu_drafts) then sd_pdraft_prepare's from pos0 on (out_tokens
  * and num_accepted are this call's own outputs), with one workspace of at least
@@ -421,6 +430,25 @@ SD_API int sd_race_E_approx_error(uint32_t w_begin, uint64_t count, float* max_r
  * from the double path's fp32(-log((w + 0.5) * 2^-32)), and to counts[1] the words that took
  * the double path. */
 SD_API int sd_race_E_check(uint32_t w_begin, uint64_t count, uint64_t* counts, void* stream);
+
+/* sd_verify_prepare with its single launch's wait made to run out (test support for the
+ * bounded wait; same arguments from B on): in the single launch, request withhold_request's
+ * rebuild CTA publishes its first drafter slot only after the CTA completing that request's race
+ * row has polled for wait_us microseconds (1..10^6) of the GPU clock and given up, so that the
+ * call raises SD_ERR_WAIT and leaves that request's final token unwritten in input_ids while
+ * every other output matches sd_verify_prepare's. Batches that take two kernels run as
+ * sd_verify_prepare does (they have no wait). Returns SD_E_SHAPE for a request outside [0, B) or
+ * wait_us outside the range. */
+SD_API int sd_diag_verify_prepare_withheld(
+    int withhold_request, uint32_t wait_us, int B, int K, int V, int dtype, const void* target,
+    long ld_t, const void* draft, long ld_d, const int32_t* drafts, const float* temperature,
+    uint64_t seed, uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
+    float* p_at_draft, float* q_at_draft, const int32_t* pos0, const int32_t* block_table,
+    int max_blocks, int block_size, int32_t mask_token_id, int capacity, int32_t* input_ids,
+    int32_t* positions, int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked,
+    uint8_t* is_rejected, int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
+    const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
+    long ld_out, void* workspace, size_t workspace_bytes, int32_t* err, void* stream);
 
 /* Text for a status code (static storage). */
 SD_API const char* sd_status_string(int status);

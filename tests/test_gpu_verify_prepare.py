@@ -183,3 +183,60 @@ def test_unaligned_rows_and_ragged_vocabulary():
     assert int(got["err"].item()) == 0
     ref = oracle.verify_probs(p.reshape(B, K + 1, V), q.reshape(B, K, V), d, seed=w.seed)
     assert np.array_equal(got["out_tokens"].cpu().numpy(), ref["out_tokens"])
+
+
+@pytest.mark.parametrize("withhold", [0, 37, 63])
+def test_bounded_wait_runs_out_cleanly(withhold):
+    # The single launch's one wait: the CTA completing a request's race row polls for the first
+    # drafter slot the request's rebuild CTA publishes. The diagnostic entry holds one request's
+    # publication back until that wait has run out (500 us of the GPU clock): the call must raise
+    # SD_ERR_WAIT, leave only that request's final drafter token unwritten, leave the workspace
+    # zeroed, and the next call must be whole again. Nothing faults, traps or hangs.
+    w = workloads.make("b64", device="cuda")
+    assert sd.sd_verify_prepare_kernels(w.B, w.K, w.V, sd.SD_F32_PROBS, False) == 1
+    cap = w.capacity
+    ws = new_ws(w.B)
+    want = run_separate(w, None, cap)
+    o = outputs(w, cap)
+    sd.sd_verify_prepare(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"], w.pos0,
+                         w.block_table, w.block_size, w.mask_token_id, o["input_ids"],
+                         o["positions"], o["slot_mapping"], o["hidden_map"], o["is_masked"],
+                         o["is_rejected"], o["start_loc"], o["new_token_idx"], o["total_out"],
+                         w.hidden, w.h_shared, o["out_hidden"], seed=w.seed,
+                         p_at_draft=o["p_at_draft"], q_at_draft=o["q_at_draft"], err=o["err"],
+                         workspace_buf=ws, diag_withhold=(withhold, 500))
+    torch.cuda.synchronize()
+    assert int(o["err"].item()) == sd.SD_ERR_WAIT
+    assert int(ws.count_nonzero()) == 0
+    g = int(want["start_loc"][withhold]) + int(want["num_accepted"][withhold])
+    ids = want["input_ids"].clone()
+    ids[g] = 77  # the prefill: the withheld request's final token is not written
+    assert torch.equal(o["input_ids"], ids)
+    for k in o:
+        if k not in ("input_ids", "err"):
+            x, y = o[k], want[k]
+            if x.dtype == torch.bfloat16:
+                x, y = x.view(torch.int16), y.view(torch.int16)
+            assert torch.equal(x, y), k
+    got = run_fused(w, None, cap, ws)
+    assert_same(got, want)
+    assert int(ws.count_nonzero()) == 0
+
+
+def test_withheld_diagnostic_without_a_wait():
+    # batches that take two kernels have no wait: the diagnostic entry then writes what
+    # sd_verify_prepare writes, with no error
+    w = workloads.make("b64", device="cuda", B=16)
+    T = w.temperature
+    assert sd.sd_verify_prepare_kernels(w.B, w.K, w.V, sd.SD_F32_PROBS, True) == 2
+    want = run_separate(w, T, w.capacity)
+    o = outputs(w, w.capacity)
+    sd.sd_verify_prepare(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"], w.pos0,
+                         w.block_table, w.block_size, w.mask_token_id, o["input_ids"],
+                         o["positions"], o["slot_mapping"], o["hidden_map"], o["is_masked"],
+                         o["is_rejected"], o["start_loc"], o["new_token_idx"], o["total_out"],
+                         w.hidden, w.h_shared, o["out_hidden"], temperature=T, seed=w.seed,
+                         p_at_draft=o["p_at_draft"], q_at_draft=o["q_at_draft"], err=o["err"],
+                         workspace_buf=new_ws(w.B), diag_withhold=(3, 500))
+    torch.cuda.synchronize()
+    assert_same(o, want)

@@ -36,7 +36,7 @@ EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
             "sd_verify_ragged", "sd_pdraft_prepare_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_race_E_check", "sd_status_string", "sd_version",
             "sd_verify_prepare", "sd_verify_prepare_workspace_bytes", "sd_verify_prepare_kernels",
-            "sd_verify_prepare_ragged"]
+            "sd_verify_prepare_ragged", "sd_diag_verify_prepare_withheld"]
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +77,8 @@ def load():
                                           P, P, P, P, P, P, i32, P, i64, i32, P, P, i64, P,
                                           ctypes.c_size_t, P, P]
         lib.sd_verify_prepare.restype = i32
+        lib.sd_diag_verify_prepare_withheld.argtypes = [i32, u32] + lib.sd_verify_prepare.argtypes
+        lib.sd_diag_verify_prepare_withheld.restype = i32
         lib.sd_verify_prepare_ragged.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, P, u64,
                                                  u32, P, P, P, P, P, P, i32, i32, ctypes.c_int32,
                                                  i32, P, P, P, P, P, P, P, P, P, i32, P, i64, i32,
@@ -215,10 +217,11 @@ def sd_verify_prepare(target, draft, drafts, out_tokens, num_accepted, pos0, blo
                       is_masked, is_rejected, start_loc, new_token_idx, total_out, target_hidden,
                       h_shared, out_hidden, temperature=None, seed=0, p_at_draft=None,
                       q_at_draft=None, err=None, stream=None, workspace_buf=None,
-                      request_base=0):
+                      request_base=0, diag_withhold=None):
     """sd_verify then sd_pdraft_prepare on its outputs, in one call (see include/sd.h): arguments
     as for the two calls; workspace_buf: zeroed uint8 device tensor of at least
-    sd_verify_prepare_workspace_bytes(B) bytes, or None for this device's shared one."""
+    sd_verify_prepare_workspace_bytes(B) bytes, or None for this device's shared one.
+    diag_withhold: test support, (request, wait_us) for sd_diag_verify_prepare_withheld."""
     import torch
 
     B, K = drafts.shape
@@ -238,8 +241,12 @@ def sd_verify_prepare(target, draft, drafts, out_tokens, num_accepted, pos0, blo
         raise SDError("out_hidden must have one row per drafter slot")
     ws = workspace_buf if workspace_buf is not None else workspace(_device(target), B, K, V,
                                                                    dtype)
-    rc = load().sd_verify_prepare(
-        B, K, V, dtype, _ptr(target), _row_stride(target), _ptr(draft), _row_stride(draft),
+    lib = load()
+    fn, pre = lib.sd_verify_prepare, ()
+    if diag_withhold is not None:
+        fn, pre = lib.sd_diag_verify_prepare_withheld, tuple(diag_withhold)
+    rc = fn(
+        *pre, B, K, V, dtype, _ptr(target), _row_stride(target), _ptr(draft), _row_stride(draft),
         _ptr(drafts), _ptr(temperature), seed, request_base, _ptr(out_tokens),
         _ptr(num_accepted), _ptr(p_at_draft), _ptr(q_at_draft), _ptr(pos0), _ptr(block_table),
         block_table.shape[1], block_size, mask_token_id, cap, _ptr(input_ids), _ptr(positions),

@@ -38,6 +38,14 @@ int sd_verify_prepare_launch(int, int, int, int, const void*, long, const void*,
                              int, int32_t*, int32_t*, int32_t*, int32_t*, uint8_t*, uint8_t*,
                              int32_t*, int32_t*, int32_t*, int, const void*, long, int,
                              const void*, void*, long, void*, int32_t*, cudaStream_t);
+int sd_verify_prepare_withheld_launch(int, uint32_t, int, int, int, int, const void*, long,
+                                      const void*, long, const int32_t*, const int32_t*,
+                                      const float*, uint64_t, uint32_t, int32_t*, int32_t*,
+                                      float*, float*, const int32_t*, const int32_t*, int, int,
+                                      int32_t, int, int32_t*, int32_t*, int32_t*, int32_t*,
+                                      uint8_t*, uint8_t*, int32_t*, int32_t*, int32_t*, int,
+                                      const void*, long, int, const void*, void*, long, void*,
+                                      int32_t*, cudaStream_t);
 int sd_verify_prepare_kernel_count(int, int, int, int, int);
 }
 
@@ -388,7 +396,7 @@ int verify_prepare(int B, int K, int V, int dtype, const void* target, long ld_t
                    int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
                    const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared,
                    void* out_hidden, long ld_out, void* workspace, size_t workspace_bytes,
-                   int32_t* err, void* stream) {
+                   int32_t* err, void* stream, int withhold = -1, uint32_t wait_us = 0) {
   // sd_verify's checks
   if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
   if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
@@ -422,6 +430,14 @@ int verify_prepare(int B, int K, int V, int dtype, const void* target, long ld_t
   if ((uintptr_t)workspace % 16) return SD_E_ALIGN;
   rc = check_device();
   if (rc != SD_OK) return rc;
+  if (withhold >= 0)
+    return sd_verify_prepare_withheld_launch(
+        withhold, wait_us, B, K, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts,
+        temperature, seed, request_base, out_tokens, num_accepted, p_at_draft, q_at_draft, pos0,
+        block_table, max_blocks, block_size, mask_token_id, capacity, input_ids, positions,
+        slot_mapping, hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out, H,
+        target_hidden, ld_in, n_in_rows, h_shared, capacity == 0 ? nullptr : out_hidden, ld_out,
+        workspace, err, (cudaStream_t)stream);
   return sd_verify_prepare_launch(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts,
                                   temperature, seed, request_base, out_tokens, num_accepted,
                                   p_at_draft, q_at_draft, pos0, block_table, max_blocks, block_size,
@@ -453,6 +469,32 @@ int sd_verify_prepare(int B, int K, int V, int dtype, const void* target, long l
                         input_ids, positions, slot_mapping, hidden_map, is_masked, is_rejected,
                         start_loc, new_token_idx, total_out, H, target_hidden, ld_in, n_in_rows,
                         h_shared, out_hidden, ld_out, workspace, workspace_bytes, err, stream);
+}
+
+int sd_diag_verify_prepare_withheld(int withhold_request, uint32_t wait_us, int B, int K, int V,
+                                    int dtype, const void* target, long ld_t, const void* draft,
+                                    long ld_d, const int32_t* drafts, const float* temperature,
+                                    uint64_t seed, uint32_t request_base, int32_t* out_tokens,
+                                    int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+                                    const int32_t* pos0, const int32_t* block_table,
+                                    int max_blocks, int block_size, int32_t mask_token_id,
+                                    int capacity, int32_t* input_ids, int32_t* positions,
+                                    int32_t* slot_mapping, int32_t* hidden_map,
+                                    uint8_t* is_masked, uint8_t* is_rejected,
+                                    int32_t* start_loc, int32_t* new_token_idx,
+                                    int32_t* total_out, int H, const void* target_hidden,
+                                    long ld_in, int n_in_rows, const void* h_shared,
+                                    void* out_hidden, long ld_out, void* workspace,
+                                    size_t workspace_bytes, int32_t* err, void* stream) {
+  if (withhold_request < 0 || withhold_request >= B || wait_us < 1 || wait_us > 1000000)
+    return SD_E_SHAPE;
+  return verify_prepare(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, nullptr, temperature,
+                        seed, request_base, out_tokens, num_accepted, p_at_draft, q_at_draft,
+                        pos0, block_table, max_blocks, block_size, mask_token_id, capacity,
+                        input_ids, positions, slot_mapping, hidden_map, is_masked, is_rejected,
+                        start_loc, new_token_idx, total_out, H, target_hidden, ld_in, n_in_rows,
+                        h_shared, out_hidden, ld_out, workspace, workspace_bytes, err, stream,
+                        withhold_request, wait_us);
 }
 
 int sd_verify_prepare_ragged(int B, int K_max, int V, int dtype, const void* target, long ld_t,

@@ -326,9 +326,14 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) {
   return __uint_as_float(b16 << 16);
 }
 
+// The GPU's nanosecond clock (%globaltimer), for waits bounded by time.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Error bits are rare; one atomic per affected request.
-// Polls a spin-wait may make before it gives up (SD_ERR_WAIT).
-constexpr uint32_t kWaitLimit = 1u << 20;
 
 __device__ __forceinline__ void raise_err(int32_t* err, int32_t bits) {
   if (err && bits) atomicOr(err, bits);

@@ -69,8 +69,18 @@ constexpr float kSkip = (1.0f + kBand) * (1.0f + 0x1p-9f);
 struct RaceSlot {
   unsigned long long best;
   unsigned int count;
-  unsigned int off1;  // fused rebuild: request r's first drafter slot + 1 once written, else 0
+  // Fused launch only: 0 until the rebuild CTA publishes request r's first drafter slot + 1, or
+  // kGaveUp once the CTA that completed r's race row stopped waiting for it. Whichever of the
+  // two CTAs comes second puts it back to 0, so every launch leaves it at 0.
+  unsigned int off1;
 };
+constexpr unsigned kGaveUp = 0xFFFFFFFFu;
+// The completing race CTA waits for the published slot at most this long (and at least
+// kMinPolls polls, so that a context switch in mid-wait does not end it early); in the fused
+// launch every CTA is resident from the start and the slot appears microseconds after it, so
+// running out means the rebuild CTA was kept off the GPU (SD_ERR_WAIT).
+constexpr uint64_t kWaitNs = 20000000ull;  // 20 ms
+constexpr uint32_t kMinPolls = 1024;
 
 // The drafter-batch rebuild fused into the verify launch (sd_verify_prepare): the same outputs
 // as the rebuild kernel, written by one extra CTA per request while the others race.
@@ -125,6 +135,9 @@ struct VerifyParams {
   int fuse;  // 1: CTAs [0, B) rebuild the drafter batch, CTAs [B, grid) race (spread over the
              // requests as evenly as they go)
   RebuildArgs rb;
+  uint64_t wait_ns;  // bound of the completing race CTA's wait for the published slot
+  int withhold;      // diagnostic (-1: none): this request's rebuild CTA publishes its slot only
+                     // once the race CTA has given up waiting, so that the wait runs out
 };
 
 // Request r's rows: K_r drafts (cu[r+1] - cu[r] when per-request counts are given, clamped to
@@ -1155,10 +1168,6 @@ __device__ __noinline__ uint32_t finish_sampled(const VerifyParams& P, int r, in
 }
 
 // ------------------------------------------------------------------------- fused rebuild
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Sum over the CTA (every thread gets it).
 __device__ long long block_sum_ll(long long v, Smem& sm) {
 #pragma unroll
@@ -1223,7 +1232,16 @@ __device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm
   if (t < KM) R.new_token_idx[(size_t)r * KM + t] = t < K ? (int32_t)(off + a + t) : -1;
   if (t == 0) {
     R.start_loc[r] = (int32_t)off;
-    st_release_u32(&P.slots[r].off1, (unsigned)(off + 1));
+    unsigned* slot = &P.slots[r].off1;
+    if (r == P.withhold) {
+      // diagnostic: hold the publication back until the race CTA has given up (bounded)
+      const uint64_t t0 = globaltimer_ns();
+      while (*(volatile unsigned*)slot != kGaveUp &&
+             globaltimer_ns() - t0 < 4 * P.wait_ns + 50000000ull) {
+      }
+    }
+    // publish, unless the completing race CTA already gave up: then put the slot back to 0
+    if (atomicCAS(slot, 0u, (unsigned)(off + 1)) == kGaveUp) atomicExch(slot, 0u);
   }
   if (R.out_hidden) {
     const long long nrows = min((long long)L, (long long)R.capacity - off);
@@ -1246,7 +1264,8 @@ __device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm
 
 // The CTA that completed request r's race row in the fused launch: the verify outputs (as
 // write_request) and the final token at slot a_r of the drafter batch, at the first slot the
-// rebuild CTA published (long before any race row completes; the wait is bounded all the same).
+// rebuild CTA published (long before any race row completes; the wait is bounded by time all
+// the same, and if it runs out the token is not written and SD_ERR_WAIT is raised).
 // tok_pre (thread t < K: draft t) and off_pre (thread 0: the published slot + 1, or 0 if not yet
 // seen) were read before the merge, so that their round trips overlap the merge's. No acquire is
 // needed: the CTA reads nothing else the rebuild CTA wrote, and writes a slot it leaves alone.
@@ -1262,16 +1281,28 @@ __device__ __noinline__ void fused_finish(const VerifyParams& P, int r, int a, i
   }
   if (t == 0) {
     P.num_accepted[r] = a;
-    volatile unsigned* slot = &P.slots[r].off1;
+    unsigned* slot = &P.slots[r].off1;
     unsigned v = off_pre;
-    for (uint32_t it = 0; v == 0u && it < kWaitLimit; ++it) v = *slot;
+    if (v == 0u) {
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t it = 0;; ++it) {
+        v = *(volatile unsigned*)slot;
+        if (v != 0u) break;
+        if (it >= kMinPolls && globaltimer_ns() - t0 > P.wait_ns) {
+          // give up, unless the slot was published in the meantime; the rebuild CTA then sees
+          // kGaveUp and puts the slot back to 0
+          v = atomicCAS(slot, 0u, kGaveUp);
+          break;
+        }
+      }
+    }
     if (v == 0u) {
       e |= SD_ERR_WAIT;
     } else {
       // slot a_r exists when the request has drafter slots at all (K_r > 0: L_r = a_r + K_r)
       const long long g = (long long)v - 1 + a;
       if (req_rows(P, r).k > 0 && g < P.rb.capacity) P.rb.input_ids[g] = (int32_t)b;
-      *slot = 0u;
+      atomicExch(slot, 0u);
     }
     raise_err(P.err, e);
   }
@@ -1703,6 +1734,25 @@ int sm_count() {
   return n;
 }
 
+// CTAs of the fp32 verify kernel that the device holds at once (occupancy query × SMs): the fused
+// launch needs every one of its CTAs resident together.
+int resident_f32() {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> cached[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  int n = cached[dev].load();
+  if (n == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, sdk::verify_kernel<SD_F32_PROBS>, sdk::NT, 0) != cudaSuccess)
+      per_sm = 0;
+    n = per_sm > 0 ? per_sm * sm_count() : -1;
+    cached[dev].store(n);
+  }
+  return n > 0 ? n : 0;
+}
+
 int choose_cluster(int V, int epu) {
   const long units = ((long)V + epu - 1) / epu;
   int cl = sdk::CL_MAX;
@@ -1757,7 +1807,7 @@ static VerifyShape verify_shape(int B, int V, int dtype, bool has_temperature) {
   // batch and at least as many racing (the race CTAs wait for the rebuild CTAs' published slots
   // only at their very end, and every CTA of the wave is resident from the start).
   v.fusable = v.race_blocks == 0 && v.cl == 1 && dtype == SD_F32_PROBS && !has_temperature &&
-              B <= sdk::kMaxFuseB && 2L * B <= (long)sdk::kMinBlocksF32 * sm_count();
+              B <= sdk::kMaxFuseB && 2L * B <= (long)resident_f32();
   return v;
 }
 
@@ -1769,7 +1819,7 @@ static int verify_launch_impl(int B, int K, int V, int dtype, const void* target
                               uint32_t request_base, int32_t* out_tokens, int32_t* num_accepted,
                               float* p_at_draft, float* q_at_draft, void* workspace,
                               int32_t* err, cudaStream_t stream, const sdk::RebuildArgs* rb,
-                              bool* fused) {
+                              bool* fused, uint64_t wait_ns = sdk::kWaitNs, int withhold = -1) {
   const int esize = dtype == SD_F32_PROBS ? 4 : 2;
   sdk::VerifyParams P;
   memset(&P, 0, sizeof(P));
@@ -1799,12 +1849,14 @@ static int verify_launch_impl(int B, int K, int V, int dtype, const void* target
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
   P.fuse = rb != nullptr && shape.fusable;
+  P.wait_ns = wait_ns;
+  P.withhold = withhold;
   if (P.fuse) {
     // B rebuild CTAs, then up to one wave's worth of race CTAs, no more per request than a row
     // splits into (every race CTA gets at least 2 NT units)
     P.rb = *rb;
     const long per = std::max(1, ((V + 3) / 4) / (2 * sdk::NT));
-    const long race = std::min((long)sdk::kMinBlocksF32 * sm_count() - B, (long)B * per);
+    const long race = std::min((long)resident_f32() - B, (long)B * per);
     P.cluster_blocks = (int)(B + race);
   }
   if (fused) *fused = P.fuse != 0;
@@ -1876,7 +1928,7 @@ extern "C" int sd_prep_launch(int B, int K, const int32_t* out_tokens, const int
 // else the verify kernel and then the rebuild kernel (the same outputs either way). The
 // workspace holds the B merge slots (each also carries its request's first drafter slot from the
 // rebuild CTA to the CTA that writes the final token).
-extern "C" int sd_verify_prepare_launch(
+static int verify_prepare_impl(
     int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
     const int32_t* drafts, const int32_t* cu_drafts, const float* temperature, uint64_t seed,
     uint32_t request_base,
@@ -1886,7 +1938,8 @@ extern "C" int sd_verify_prepare_launch(
     int32_t* slot_mapping, int32_t* hidden_map, uint8_t* is_masked, uint8_t* is_rejected,
     int32_t* start_loc, int32_t* new_token_idx, int32_t* total_out, int H,
     const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
-    long ld_out, void* workspace, int32_t* err, cudaStream_t stream) {
+    long ld_out, void* workspace, int32_t* err, cudaStream_t stream, uint64_t wait_ns,
+    int withhold) {
   sdk::RebuildArgs rb;
   rb.pos0 = pos0;
   rb.block_table = block_table;
@@ -1916,13 +1969,43 @@ extern "C" int sd_verify_prepare_launch(
   bool fused = false;
   int rc = verify_launch_impl(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts,
                               temperature, seed, request_base, out_tokens, num_accepted,
-                              p_at_draft, q_at_draft, workspace, err, stream, &rb, &fused);
+                              p_at_draft, q_at_draft, workspace, err, stream, &rb, &fused,
+                              wait_ns, withhold);
   if (rc != SD_OK || fused) return rc;
   return sd_prep_launch(B, K, out_tokens, num_accepted, cu_drafts, pos0, block_table, max_blocks,
                         block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,
                         hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out,
                         H, target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
                         stream);
+}
+
+#define SD_VERIFY_PREPARE_PARAMS                                                                \
+  int B, int K, int V, int dtype, const void *target, long ld_t, const void *draft, long ld_d, \
+      const int32_t *drafts, const int32_t *cu_drafts, const float *temperature,               \
+      uint64_t seed, uint32_t request_base, int32_t *out_tokens, int32_t *num_accepted,        \
+      float *p_at_draft, float *q_at_draft, const int32_t *pos0, const int32_t *block_table,   \
+      int max_blocks, int block_size, int32_t mask_token_id, int capacity, int32_t *input_ids, \
+      int32_t *positions, int32_t *slot_mapping, int32_t *hidden_map, uint8_t *is_masked,      \
+      uint8_t *is_rejected, int32_t *start_loc, int32_t *new_token_idx, int32_t *total_out,    \
+      int H, const void *target_hidden, long ld_in, int n_in_rows, const void *h_shared,       \
+      void *out_hidden, long ld_out, void *workspace, int32_t *err, cudaStream_t stream
+#define SD_VERIFY_PREPARE_ARGS                                                                 \
+  B, K, V, dtype, target, ld_t, draft, ld_d, drafts, cu_drafts, temperature, seed,             \
+      request_base, out_tokens, num_accepted, p_at_draft, q_at_draft, pos0, block_table,       \
+      max_blocks, block_size, mask_token_id, capacity, input_ids, positions, slot_mapping,     \
+      hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out, H,              \
+      target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, workspace, err, stream
+
+extern "C" int sd_verify_prepare_launch(SD_VERIFY_PREPARE_PARAMS) {
+  return verify_prepare_impl(SD_VERIFY_PREPARE_ARGS, sdk::kWaitNs, -1);
+}
+
+// Diagnostic form: in the fused launch, request `withhold`'s rebuild CTA publishes its first
+// drafter slot only after the completing race CTA has waited wait_us microseconds and given up
+// (SD_ERR_WAIT), so that a test can run the wait out without a fault.
+extern "C" int sd_verify_prepare_withheld_launch(int withhold, uint32_t wait_us,
+                                                 SD_VERIFY_PREPARE_PARAMS) {
+  return verify_prepare_impl(SD_VERIFY_PREPARE_ARGS, (uint64_t)wait_us * 1000ull, withhold);
 }
 
 // Kernels one sd_verify_prepare call launches.
