@@ -283,19 +283,24 @@ struct F32ResidualAny {
   }
 };
 
-// p(x) = exp2((l - M) * c) / S with c = log2(e) / T, written with explicit roundings so that the
-// streamed pass and the scalar re-evaluation of a candidate give the same bits.
-__device__ __forceinline__ float logit_prob(float l, float M, float c, float invS) {
-  return __fmul_rn(fast_ex2(__fmul_rn(__fsub_rn(l, M), c)), invS);
+// p(x) = exp2(l c - ref c) / S with c = log2(e) / T and S the row's sum of the same terms for a
+// fixed reference logit ref (nrc = -(ref c)); written with explicit roundings so that the
+// streamed statistics, the streamed race and the scalar re-evaluation of a candidate give the
+// same bits for the same element.
+__device__ __forceinline__ float logit_term(float l, float c, float nrc) {
+  return fast_ex2(fmaf(l, c, nrc));
+}
+__device__ __forceinline__ float logit_prob(float l, float c, float nrc, float invS) {
+  return __fmul_rn(logit_term(l, c, nrc), invS);
 }
 
 template <bool HAS_Q>
 struct Bf16Residual {
   static constexpr int EPU = 8;
-  static constexpr int UNR = 1;  // one unit in flight: no spills at the kernel's 64 registers
+  static constexpr int UNR = 1;  // one unit in flight: no spills at the kernel's 48 registers
   const uint16_t* t;
   const uint16_t* d;
-  float Mt, invSt, Md, invSd, c;
+  float nrct, invSt, nrcd, invSd, c;
   uint32_t V;
   bool vec;
   struct Raw {
@@ -313,8 +318,8 @@ struct Bf16Residual {
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[8]) const {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float pv = logit_prob(bf16_at(raw.t, i), Mt, c, invSt);
-      r[i] = HAS_Q ? __fsub_rn(pv, logit_prob(bf16_at(raw.d, i), Md, c, invSd)) : pv;
+      const float pv = logit_prob(bf16_at(raw.t, i), c, nrct, invSt);
+      r[i] = HAS_Q ? __fsub_rn(pv, logit_prob(bf16_at(raw.d, i), c, nrcd, invSd)) : pv;
     }
   }
   // An upper bound of the unit's residuals without their exponentials: r(x) <= p(x) (q >= 0),
@@ -326,25 +331,27 @@ struct Bf16Residual {
     asm("max.bf16x2 %0, %1, %2;" : "=r"(m23) : "r"(raw.t.z), "r"(raw.t.w));
     asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(m01), "r"(m23));
     const float lmax = fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
-    return logit_prob(lmax, Mt, c, invSt);
+    return logit_prob(lmax, c, nrct, invSt);
   }
   __device__ __forceinline__ float at(uint32_t x) const {
-    const float pv = logit_prob(bf16_bits_to_float(__ldg(t + x)), Mt, c, invSt);
-    return HAS_Q ? __fsub_rn(pv, logit_prob(bf16_bits_to_float(__ldg(d + x)), Md, c, invSd)) : pv;
+    const float pv = logit_prob(bf16_bits_to_float(__ldg(t + x)), c, nrct, invSt);
+    return HAS_Q ? __fsub_rn(pv, logit_prob(bf16_bits_to_float(__ldg(d + x)), c, nrcd, invSd))
+                 : pv;
   }
 };
 
 // -------------------------------------------------------------------------------- shared state
 struct Smem {
   uint64_t red[NT / 32];
-  float redf[4][NT / 32];
+  float2 redf[2][NT / 32];  // block sums of a row pair (double-buffered by call parity)
   uint64_t slot[2];   // per-CTA cluster exchange (double-buffered)
   uint64_t slot2[2];  // second value of a paired exchange (greedy rows two at a time)
   uint64_t red2[NT / 32];
   uint64_t bcast2;
-  float4 fslot[2];
+  float2 xslot[2];    // this CTA's row sums for the cluster (row parity)
+  float2 xslot_fb;    // the same for a row's max-referenced recomputation
   uint64_t bcast;
-  float4 fbcast;
+  float lt[SD_K_MAX + 1], ld[SD_K_MAX];  // logit rows: the draft token's logits (references)
   float P[SD_K_MAX], Q[SD_K_MAX];
   int a;
   int e;
@@ -911,87 +918,37 @@ __device__ void argmax_chunk2(const void* row0, const void* row1, uint32_t V, bo
   pk1 = p1;
 }
 
-// ------------------------------------------------------------------- softmax statistics (bf16)
-struct MaxSum {
-  float m, s;
+// ------------------------------------------------------------ softmax statistics (bf16 rows)
+// Per row the cluster forms S = sum_x 2^(l_x c - ref c) for a fixed reference logit ref: the
+// draft token's own logit (element 0 of the row for the bonus row or an out-of-range draft).
+// p(x) = 2^(l_x c - ref c) / S is the softmax whatever the reference, so no running maximum is
+// kept and the partial sums combine by plain addition, in a fixed order (the results do not
+// depend on timing). Every term is at most S, so S < kRefSumLimit certifies that no term
+// overflowed; otherwise (extreme logits or temperatures) the row is summed again with the
+// row's maximum as the reference. Terms flush to 0 below 2^-126, far below the reference term.
+constexpr float kRefSumLimit = 0x1p100f;
+constexpr int kLookAhead = 4;  // the next row's first 1/kLookAhead is streamed during the exchange
+
+struct RefAcc {
+  float s = 0.0f, comp = 0.0f;  // compensated running sum
 };
 
-__device__ __forceinline__ MaxSum combine(MaxSum a, MaxSum b, float c) {
-  const float m = fmaxf(a.m, b.m);
-  if (m == -INFINITY) return MaxSum{m, 0.0f};
-  const float sa = a.m == -INFINITY ? 0.0f : a.s * fast_ex2((a.m - m) * c);
-  const float sb = b.m == -INFINITY ? 0.0f : b.s * fast_ex2((b.m - m) * c);
-  return MaxSum{m, sa + sb};
-}
-
-__device__ __forceinline__ void absorb_unit(MaxSum& st, float& comp, const uint4& raw, float c) {
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = bf16_at(raw, i);
-  float um = v[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) um = fmaxf(um, v[i]);
-  if (um > st.m) {
-    if (st.m != -INFINITY) {
-      const float f = fast_ex2((st.m - um) * c);
-      st.s *= f;
-      comp *= f;
-    }
-    st.m = um;
-  }
-  if (st.m == -INFINITY) return;
+__device__ __forceinline__ void absorb_ref(RefAcc& a, const uint4& raw, float c, float nrc) {
   float e[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) e[i] = fast_ex2((v[i] - st.m) * c);
+  for (int i = 0; i < 8; ++i) e[i] = logit_term(bf16_at(raw, i), c, nrc);
   const float part = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-  // compensated running sum
-  const float y = part - comp;
-  const float t = st.s + y;
-  comp = (t - st.s) - y;
-  st.s = t;
+  const float y = part - a.comp;
+  const float t = a.s + y;
+  a.comp = (t - a.s) - y;
+  a.s = t;
 }
 
-__device__ void block_maxsum2(MaxSum& a, MaxSum& b, float c, Smem& sm) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    MaxSum ao{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
-    MaxSum bo{__shfl_xor_sync(0xffffffffu, b.m, o), __shfl_xor_sync(0xffffffffu, b.s, o)};
-    a = combine(a, ao, c);
-    b = combine(b, bo, c);
-  }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) {
-    sm.redf[0][warp] = a.m;
-    sm.redf[1][warp] = a.s;
-    sm.redf[2][warp] = b.m;
-    sm.redf[3][warp] = b.s;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    a = lane < NT / 32 ? MaxSum{sm.redf[0][lane], sm.redf[1][lane]} : MaxSum{-INFINITY, 0.0f};
-    b = lane < NT / 32 ? MaxSum{sm.redf[2][lane], sm.redf[3][lane]} : MaxSum{-INFINITY, 0.0f};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      MaxSum ao{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
-      MaxSum bo{__shfl_xor_sync(0xffffffffu, b.m, o), __shfl_xor_sync(0xffffffffu, b.s, o)};
-      a = combine(a, ao, c);
-      b = combine(b, bo, c);
-    }
-    if (lane == 0) sm.fbcast = make_float4(a.m, a.s, b.m, b.s);
-  }
-  __syncthreads();
-  a = MaxSum{sm.fbcast.x, sm.fbcast.y};
-  b = MaxSum{sm.fbcast.z, sm.fbcast.w};
-}
-
-// Row statistics of target row and (if HAS_Q) draft row, combined over the cluster.
+// Units [u0, u1) of target row trow (and, with HAS_Q, draft row drow) into the accumulators.
 template <bool HAS_Q>
-__device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V, bool vec,
-                          uint32_t u0, uint32_t u1, float c, MaxSum& st, MaxSum& sd, Smem& sm,
-                          int& phase, int cl) {
-  MaxSum a{-INFINITY, 0.0f}, b{-INFINITY, 0.0f};
-  float ca = 0.0f, cb = 0.0f;
+__device__ __forceinline__ void ref_sums(const uint16_t* trow, const uint16_t* drow, uint32_t V,
+                                         bool vec, uint32_t u0, uint32_t u1, float c, float nrct,
+                                         float nrcd, RefAcc& at, RefAcc& ad) {
   const uint32_t uf = vec ? max(u0, min(u1, V / 8u)) : u0;
   uint32_t ub = u0 + threadIdx.x;
   if (ub + (UNROLL - 1) * NT < uf) {  // unchecked 128-bit loads, UNROLL units always in flight
@@ -1004,45 +961,153 @@ __device__ void row_stats(const uint16_t* trow, const uint16_t* drow, uint32_t V
     for (; ub + (2 * UNROLL - 1) * NT < uf; ub += UNROLL * NT) {
 #pragma unroll
       for (int k = 0; k < UNROLL; ++k) {
-        absorb_unit(a, ca, vt[k], c);
-        if (HAS_Q) absorb_unit(b, cb, vd[k], c);
+        absorb_ref(at, vt[k], c, nrct);
+        if (HAS_Q) absorb_ref(ad, vd[k], c, nrcd);
         vt[k] = ld_stream_u4(trow + 8u * (ub + (k + UNROLL) * NT));
         if (HAS_Q) vd[k] = ld_stream_u4(drow + 8u * (ub + (k + UNROLL) * NT));
       }
     }
 #pragma unroll
     for (int k = 0; k < UNROLL; ++k) {
-      absorb_unit(a, ca, vt[k], c);
-      if (HAS_Q) absorb_unit(b, cb, vd[k], c);
+      absorb_ref(at, vt[k], c, nrct);
+      if (HAS_Q) absorb_ref(ad, vd[k], c, nrcd);
     }
     ub += UNROLL * NT;
   }
-  for (; ub < u1; ub += NT) {  // the rest, bounds-checked
-    absorb_unit(a, ca, bf16_raw(trow, ub, V, vec), c);
-    if (HAS_Q) absorb_unit(b, cb, bf16_raw(drow, ub, V, vec), c);
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked (-inf past the row end: term 0)
+    absorb_ref(at, bf16_raw(trow, ub, V, vec), c, nrct);
+    if (HAS_Q) absorb_ref(ad, bf16_raw(drow, ub, V, vec), c, nrcd);
   }
-  a.s -= ca;
-  b.s -= cb;
-  block_maxsum2(a, b, c, sm);
-  if (cl > 1) {
-    if (threadIdx.x == 0) sm.fslot[phase] = make_float4(a.m, a.s, b.m, b.s);
-    cluster_barrier();
-    if (threadIdx.x == 0) {
-      MaxSum A{-INFINITY, 0.0f}, Bm{-INFINITY, 0.0f};
-      for (int rk = 0; rk < cl; ++rk) {
-        const float4 f = load_from_rank(&sm.fslot[phase], (unsigned)rk);
-        A = combine(A, MaxSum{f.x, f.y}, c);
-        Bm = combine(Bm, MaxSum{f.z, f.w}, c);
-      }
-      sm.fbcast = make_float4(A.m, A.s, Bm.m, Bm.s);
+}
+
+// Sums of two values over the CTA, in a fixed order (every thread gets them). `par` alternates
+// between calls, so one barrier per call suffices.
+__device__ __forceinline__ float2 block_sum2(float a, float b, Smem& sm, int& par) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) sm.redf[par][warp] = make_float2(a, b);
+  __syncthreads();
+  float2 t = sm.redf[par][0];
+#pragma unroll
+  for (int w = 1; w < NT / 32; ++w) {
+    t.x += sm.redf[par][w].x;
+    t.y += sm.redf[par][w].y;
+  }
+  par ^= 1;
+  return t;
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Post this CTA's row sums for the cluster and arrive (the wait comes later, in
+// cluster_collect, so that the exchange overlaps the next row's first units).
+__device__ __forceinline__ void cluster_post(float2 v, float2* slot, int cl) {
+  if (cl == 1) return;
+  if (threadIdx.x == 0) *slot = v;
+  cluster_arrive_release();
+}
+
+// Wait, then the cluster's sums (mine for cl == 1): in every warp lanes 0..cl-1 read rank
+// lane's slot and reduce in a fixed order, so every CTA gets the same bits.
+__device__ __forceinline__ float2 cluster_collect(float2 mine, float2* slot, int cl) {
+  if (cl == 1) return mine;
+  cluster_wait_acquire();
+  const int lane = threadIdx.x & 31;
+  float2 v = make_float2(0.0f, 0.0f);
+  if (lane < cl) v = load_from_rank(slot, (unsigned)lane);
+  for (int o = cl >> 1; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  v.x = __shfl_sync(0xffffffffu, v.x, 0);
+  v.y = __shfl_sync(0xffffffffu, v.y, 0);
+  return v;
+}
+
+// Largest logit of two rows over the cluster (drow may be NULL: -inf), for the max-referenced
+// recomputation of a row's sums.
+__device__ void row_max2(const uint16_t* trow, const uint16_t* drow, uint32_t V, bool vec,
+                         uint32_t u0, uint32_t u1, Smem& sm, int& phase, int cl, float& mt,
+                         float& md) {
+  float a = -INFINITY, b = -INFINITY;
+  for (uint32_t u = u0 + threadIdx.x; u < u1; u += NT) {
+    const uint4 t = bf16_raw(trow, u, V, vec);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, bf16_at(t, i));
+    if (drow) {
+      const uint4 d = bf16_raw(drow, u, V, vec);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b = fmaxf(b, bf16_at(d, i));
     }
-    __syncthreads();
-    a = MaxSum{sm.fbcast.x, sm.fbcast.y};
-    b = MaxSum{sm.fbcast.z, sm.fbcast.w};
-    phase ^= 1;
   }
-  st = a;
-  sd = b;
+  // maxima as orderable bits, over the CTA, then over the cluster
+  uint64_t pa = orderable(a), pb = orderable(b);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t xa = __shfl_xor_sync(0xffffffffu, pa, o);
+    const uint64_t xb = __shfl_xor_sync(0xffffffffu, pb, o);
+    pa = xa > pa ? xa : pa;
+    pb = xb > pb ? xb : pb;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) {
+    sm.red[warp] = pa;
+    sm.red2[warp] = pb;
+  }
+  __syncthreads();
+  pa = 0ull;
+  pb = 0ull;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    pa = sm.red[w] > pa ? sm.red[w] : pa;
+    pb = sm.red2[w] > pb ? sm.red2[w] : pb;
+  }
+  cluster_max2_u64(pa, pb, sm, phase, cl);
+  auto unorder = [](uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+  };
+  mt = unorder((uint32_t)pa);
+  md = unorder((uint32_t)pb);
+}
+
+// The race on a logit row pair (HAS_Q) or on p alone, over the cluster: out of line, so that its
+// registers do not add to the statistics loop's.
+template <bool HAS_Q>
+__device__ __noinline__ uint64_t logit_race(const uint16_t* t, const uint16_t* d, float nrct,
+                                            float invSt, float nrcd, float invSd, float c,
+                                            uint32_t V, bool vec, uint32_t u0, uint32_t u1,
+                                            const PhiloxRoundKeys& rk, uint32_t rid, uint32_t j,
+                                            Smem& sm, int& phase, int cl) {
+  const Bf16Residual<HAS_Q> src{t, d, nrct, invSt, nrcd, invSd, c, V, vec};
+  return cluster_max_u64(race_chunk(src, u0, u1, rk, rid, j, sm), sm, phase, cl);
+}
+
+// A row's sums again against the row maxima (the rare case where the draft token's logit is too
+// far below the row's largest for the terms to stay finite). Returns S and the new nrc's.
+__device__ __noinline__ float2 logit_row_refit(const uint16_t* trow, const uint16_t* drow,
+                                               uint32_t V, bool vec, uint32_t u0, uint32_t u1,
+                                               float c, Smem& sm, int& phase, int& par, int cl,
+                                               float& nrct, float& nrcd) {
+  float mt, md;
+  row_max2(trow, drow, V, vec, u0, u1, sm, phase, cl, mt, md);
+  nrct = -__fmul_rn(mt, c);
+  nrcd = drow ? -__fmul_rn(md, c) : 0.0f;
+  RefAcc ft, fd;
+  if (drow) ref_sums<true>(trow, drow, V, vec, u0, u1, c, nrct, nrcd, ft, fd);
+  else ref_sums<false>(trow, nullptr, V, vec, u0, u1, c, nrct, 0.0f, ft, fd);
+  const float2 fm = block_sum2(ft.s - ft.comp, fd.s - fd.comp, sm, par);
+  cluster_post(fm, &sm.xslot_fb, cl);
+  return cluster_collect(fm, &sm.xslot_fb, cl);
 }
 
 // -------------------------------------------------------- sampled probability requests (shared)
@@ -1434,6 +1499,20 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
     sm.P[threadIdx.x] = -1.0f;
     sm.Q[threadIdx.x] = -1.0f;
   }
+  if constexpr (DT == SD_BF16_LOGITS) {
+    // logit rows: each row's reference logits (the draft token's, element 0 when it is out of
+    // range or for the bonus row), read once before any row is streamed
+    if (!greedy && threadIdx.x <= (unsigned)K) {
+      const int j = threadIdx.x;
+      int x = 0;
+      if (j < K) {
+        const int d = __ldg(dr + j);
+        x = (d >= 0 && (uint32_t)d < V) ? d : 0;
+        sm.ld[j] = bf16_bits_to_float(__ldg((const uint16_t*)drow(j) + x));
+      }
+      sm.lt[j] = bf16_bits_to_float(__ldg((const uint16_t*)trow(j) + x));
+    }
+  }
   if (threadIdx.x == 0) sm.tau = 0u;
   __syncthreads();
 
@@ -1521,77 +1600,87 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
     }
     writer = false;  // finish_sampled wrote the outputs (in the CTA that completed the row)
   } else {
-    // ---- sampled, bf16 logit rows: per row max/sum, decide, race on the rejected row
+    // ---- sampled, bf16 logit rows: per row the sums S_t, S_d against the draft token's
+    // logits, decide, race on the rejected row (or on p_K when every draft is accepted). The
+    // cluster exchange of row j's sums overlaps the first units of row j+1.
     const float c = 1.4426950408889634f / T;
     const uint16_t* t16 = (const uint16_t*)tbase;
     const uint16_t* d16 = (const uint16_t*)dbase;
-    int jr = K;
-    bool done = false;
-    for (int j = 0; j < K; ++j) {
-      const int d = __ldg(dr + j);
-      const bool valid = d >= 0 && (uint32_t)d < V;
-      MaxSum st, sd;
-      row_stats<true>(t16 + (size_t)j * P.ld_t, d16 + (size_t)j * P.ld_d, V, vec, u0, u1, c, st,
-                      sd, sm, phase, cl);
-      bool accept = false;
-      float Pv = 0.0f, Qv = 0.0f;
-      if (valid) {
-        Pv = __fdiv_rn(exp2f(__fmul_rn(__fsub_rn(bf16_bits_to_float(
-                                                      __ldg(t16 + (size_t)j * P.ld_t + d)),
-                                                  st.m),
-                                        c)),
-                       st.s);
-        Qv = __fdiv_rn(exp2f(__fmul_rn(__fsub_rn(bf16_bits_to_float(
-                                                      __ldg(d16 + (size_t)j * P.ld_d + d)),
-                                                  sd.m),
-                                        c)),
-                       sd.s);
-        const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
-        accept = u * (double)Qv < (double)Pv;
-      } else {
-        e |= SD_ERR_TOKEN_RANGE;
+    auto tr = [&](int j) { return t16 + (size_t)j * P.ld_t; };
+    auto dq = [&](int j) { return d16 + (size_t)j * P.ld_d; };
+    // a row's references: the draft token's logits (element 0 when it is out of range; element
+    // 0 of row K for the bonus row)
+    auto nrc_of = [&](float ref) { return -__fmul_rn(ref, c); };
+    auto ref_t = [&](int j) { return sm.lt[j]; };
+    auto ref_d = [&](int j) { return sm.ld[j]; };
+    const uint32_t us = u0 + (u1 - u0) / kLookAhead;
+    int par = 0;
+    // one row's units [lo, hi): target and draft rows j < K, the target row alone for j == K
+    auto stream = [&](int j, uint32_t lo, uint32_t hi, RefAcc& at, RefAcc& ad) {
+      if (j < K)
+        ref_sums<true>(tr(j), dq(j), V, vec, lo, hi, c, nrc_of(ref_t(j)), nrc_of(ref_d(j)), at, ad);
+      else
+        ref_sums<false>(tr(j), nullptr, V, vec, lo, hi, c, nrc_of(ref_t(j)), 0.0f, at, ad);
+    };
+    RefAcc at, ad;
+    stream(0, u0, u1, at, ad);
+    float2 mine = block_sum2(at.s - at.comp, ad.s - ad.comp, sm, par);
+    cluster_post(mine, &sm.xslot[0], cl);
+    for (int j = 0;; ++j) {
+      // look-ahead: the first units of row j+1 while the cluster's sums of row j arrive
+      RefAcc nt, nd;
+      if (j + 1 <= K) stream(j + 1, u0, us, nt, nd);
+      float2 S = cluster_collect(mine, &sm.xslot[j & 1], cl);
+      float nrct = nrc_of(ref_t(j)), nrcd = j < K ? nrc_of(ref_d(j)) : 0.0f;
+      if (!(S.x < kRefSumLimit) || (j < K && !(S.y < kRefSumLimit))) {
+        // a term may have overflowed: sum the row again against its maximum (cluster-uniform)
+        S = logit_row_refit(tr(j), j < K ? dq(j) : nullptr, V, vec, u0, u1, c, sm, phase, par,
+                            cl, nrct, nrcd);
       }
-      if (threadIdx.x == 0) {
-        sm.P[j] = Pv;
-        sm.Q[j] = Qv;
+      bool accept = false;
+      if (j < K) {
+        const int d = __ldg(dr + j);
+        const bool valid = d >= 0 && (uint32_t)d < V;
+        float Pv = 0.0f, Qv = 0.0f;
+        if (valid) {
+          Pv = __fdiv_rn(logit_term(ref_t(j), c, nrct), S.x);
+          Qv = __fdiv_rn(logit_term(ref_d(j), c, nrcd), S.y);
+          const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
+          accept = u * (double)Qv < (double)Pv;
+        } else {
+          e |= SD_ERR_TOKEN_RANGE;
+        }
+        if (threadIdx.x == 0) {
+          sm.P[j] = Pv;
+          sm.Q[j] = Qv;
+        }
       }
       if (!accept) {
+        // the race on row j: the residual of the rejected pair, or p_K for the bonus token
         a = j;
-        jr = j;
-        Bf16Residual<true> src{t16 + (size_t)j * P.ld_t, d16 + (size_t)j * P.ld_d, st.m,
-                               1.0f / st.s, sd.m, 1.0f / sd.s, c, V, vec};
-        uint64_t pk = cluster_max_u64(
-            race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)j, sm), sm, phase, cl);
-        if (packed_key_bits(pk) == 0u) {
-          Bf16Residual<false> srcp{t16 + (size_t)j * P.ld_t, nullptr, st.m, 1.0f / st.s,
-                                   0.0f, 0.0f, c, V, vec};
-          pk = cluster_max_u64(race_chunk(srcp, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)j, sm),
-                               sm, phase, cl);
-        }
+        const float invSt = 1.0f / S.x;
+        uint64_t pk;
+        const uint32_t rid = P.rbase + (uint32_t)r;
+        if (j < K)
+          pk = logit_race<true>(tr(j), dq(j), nrct, invSt, nrcd, 1.0f / S.y, c, V, vec, u0, u1,
+                                P.rk, rid, (uint32_t)j, sm, phase, cl);
+        else
+          pk = 0ull;
+        if (packed_key_bits(pk) == 0u)  // the bonus race, or no positive residual: p itself
+          pk = logit_race<false>(tr(j), nullptr, nrct, invSt, 0.0f, 0.0f, c, V, vec, u0, u1, P.rk,
+                                 rid, (uint32_t)j, sm, phase, cl);
         if (packed_key_bits(pk) == 0u) {
           e |= SD_ERR_ZERO_ROW;
           b = 0;
         } else {
           b = packed_index(pk);
         }
-        done = true;
         break;
       }
-    }
-    if (!done) {
-      MaxSum st, sd;
-      row_stats<false>(t16 + (size_t)jr * P.ld_t, nullptr, V, vec, u0, u1, c, st, sd, sm, phase,
-                       cl);
-      Bf16Residual<false> src{t16 + (size_t)jr * P.ld_t, nullptr, st.m, 1.0f / st.s,
-                              0.0f, 0.0f, c, V, vec};
-      const uint64_t pk = cluster_max_u64(
-          race_chunk(src, u0, u1, P.rk, P.rbase + (uint32_t)r, (uint32_t)jr, sm), sm, phase, cl);
-      if (packed_key_bits(pk) == 0u) {
-        e |= SD_ERR_ZERO_ROW;
-        b = 0;
-      } else {
-        b = packed_index(pk);
-      }
+      // accepted: the rest of row j+1, then its sums go to the cluster
+      stream(j + 1, us, u1, nt, nd);
+      mine = block_sum2(nt.s - nt.comp, nd.s - nd.comp, sm, par);
+      cluster_post(mine, &sm.xslot[(j + 1) & 1], cl);
     }
   }
 
