@@ -58,7 +58,7 @@ constexpr int kMinBlocks = 5;
 constexpr int min_blocks(int dt) { return dt == SD_F32_PROBS ? kMinBlocksF32 : kMinBlocks; }
 constexpr int kRaceMinBlocks = 4;  // the same for race_kernel (its loop keeps 3 units in flight)
 constexpr float kBand = 1.0f / 128.0f;  // race candidate band (relative)
-constexpr int kCandCap = 32;            // candidate units evaluated lane-parallel per CTA
+constexpr int kCandCap = 32;            // candidate units evaluated thread-parallel per CTA
 constexpr int kMaxSeg = NT / 32;        // requests one race-kernel CTA may touch (a warp each)
 // A unit whose bound r_max * R(w_max) * kSkip stays below the CTA's running best is skipped (see
 // race_take): (1 + kBand) for the filter's band, 2^-9 for the approximations inside the bound.
@@ -204,6 +204,7 @@ template <bool HAS_Q>
 struct F32Residual {
   static constexpr int EPU = 4;
   static constexpr int UNR = 2;  // units in flight per thread
+  static constexpr bool kLean = false;
   const float* p;
   const float* q;
   uint32_t V;
@@ -225,6 +226,8 @@ struct F32Residual {
       raw.q[0] = b.x; raw.q[1] = b.y; raw.q[2] = b.z; raw.q[3] = b.w;
     }
   }
+  // the rest of a unit fetched by fetch_fast (here nothing: both rows are in)
+  __device__ __forceinline__ void complete(uint32_t, Raw&) const {}
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[4]) const {
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[i] = HAS_Q ? __fsub_rn(raw.p[i], raw.q[i]) : raw.p[i];
@@ -245,6 +248,7 @@ struct F32Residual {
 struct F32ResidualAny {
   static constexpr int EPU = 4;
   static constexpr int UNR = 3;
+  static constexpr bool kLean = false;
   const float* p;
   const float* q;  // nullptr: r = p
   uint32_t V;
@@ -268,6 +272,7 @@ struct F32ResidualAny {
       raw.q[0] = raw.q[1] = raw.q[2] = raw.q[3] = 0.0f;
     }
   }
+  __device__ __forceinline__ void complete(uint32_t, Raw&) const {}
   // p - 0 == p exactly, so the bonus race sees r = p as the definition asks
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[4]) const {
 #pragma unroll
@@ -297,7 +302,8 @@ __device__ __forceinline__ float logit_prob(float l, float c, float nrc, float i
 template <bool HAS_Q>
 struct Bf16Residual {
   static constexpr int EPU = 8;
-  static constexpr int UNR = 1;  // one unit in flight: no spills at the kernel's 48 registers
+  static constexpr int UNR = 1;  // target units in flight per thread
+  static constexpr bool kLean = true;
   const uint16_t* t;
   const uint16_t* d;
   float nrct, invSt, nrcd, invSd, c;
@@ -311,8 +317,12 @@ struct Bf16Residual {
     if (HAS_Q) raw.d = bf16_raw(d, u, V, vec);
   }
   __device__ __forceinline__ uint32_t full_units() const { return V / 8u; }
+  // The streamed pass reads the target unit alone: the skip bound needs only p (r <= p, as
+  // q >= 0), and the draft unit is read (complete) for the units that pass it.
   __device__ __forceinline__ void fetch_fast(uint32_t u, Raw& raw) const {
     raw.t = ld_stream_u4(t + 8u * u);
+  }
+  __device__ __forceinline__ void complete(uint32_t u, Raw& raw) const {
     if (HAS_Q) raw.d = ld_stream_u4(d + 8u * u);
   }
   __device__ __forceinline__ void residual(const Raw& raw, float (&r)[8]) const {
@@ -492,13 +502,40 @@ __device__ __noinline__ void exact_unit(const Src& src, uint32_t u, const Philox
 // the word, so R(w_max) bounds R(w_x) of the unit up to the approximation error) stays below
 // max(a1, *tau) has m * (1 + kBand) < A: it cannot be a candidate, and skipping it changes
 // neither A nor a thread's candidate units; its keys are not computed.
+// The largest Philox word of unit u: all the skip bound needs (the words themselves are
+// recomputed for the few units that pass it, so that they need no registers in the loop).
+template <int EPU>
+__device__ __forceinline__ uint32_t unit_wmax_of(const PhiloxRoundKeys& rk, uint32_t u,
+                                                 uint32_t rid, uint32_t j, uint32_t tag) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int h = 0; h < EPU / 4; ++h) {
+    const uint4 w = race_block(rk, u * (EPU / 4) + h, rid, j, tag);
+    m = max(m, max(max(w.x, w.y), max(w.z, w.w)));
+  }
+  return m;
+}
+
 template <class Src>
-__device__ __forceinline__ void race_take(const Src& src, const typename Src::Raw& raw,
-                                          const uint4 (&w)[Src::EPU / 4], uint32_t u, float& a1,
-                                          float& a2, uint32_t& best_u, uint32_t* tau) {
-  const uint32_t wmax = unit_wmax<Src::EPU>(w);
+__device__ __forceinline__ void race_take(const Src& src, typename Src::Raw& raw,
+                                          const PhiloxRoundKeys& rk, uint32_t rid, uint32_t j,
+                                          uint32_t tag, uint32_t u, float& a1, float& a2,
+                                          uint32_t& best_u, uint32_t* tau, bool fetched = false) {
+  // Logit rows (two Philox blocks per unit) keep only the largest word through the bound and
+  // recompute the words for the units that pass it, which keeps the loop's registers down;
+  // probability rows (one block per unit) keep the words.
+  uint4 w[Src::EPU / 4];
+  uint32_t wmax;
+  if (Src::kLean) {
+    wmax = unit_wmax_of<Src::EPU>(rk, u, rid, j, tag);
+  } else {
+    unit_words<Src>(rk, u, rid, j, tag, w);
+    wmax = unit_wmax<Src::EPU>(w);
+  }
   const float thr = fmaxf(a1, __uint_as_float(*(volatile uint32_t*)tau));
   if (src.residual_bound(raw) * race_R(wmax) * kSkip < thr) return;
+  if (!fetched) src.complete(u, raw);
+  if (Src::kLean) unit_words<Src>(rk, u, rid, j, tag, w);
   float r[Src::EPU];
   src.residual(raw, r);
   const float m = unit_max_alpha<Src::EPU>(r, w, wmax);
@@ -529,27 +566,21 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
 #pragma unroll
       for (int k = 0; k < UNR; ++k) {
         const uint32_t u = ub + k * NT;
-        uint4 w[EPU / 4];
-        unit_words<Src>(rk, u, rid, j, tag, w);
-        race_take(src, raw[k], w, u, a1, a2, best_u, &sm.tau);
+        race_take(src, raw[k], rk, rid, j, tag, u, a1, a2, best_u, &sm.tau);
         src.fetch_fast(u + UNR * NT, raw[k]);
       }
     }
 #pragma unroll
     for (int k = 0; k < UNR; ++k) {  // drain the last UNR units in flight
       const uint32_t u = ub + k * NT;
-      uint4 w[EPU / 4];
-      unit_words<Src>(rk, u, rid, j, tag, w);
-      race_take(src, raw[k], w, u, a1, a2, best_u, &sm.tau);
+      race_take(src, raw[k], rk, rid, j, tag, u, a1, a2, best_u, &sm.tau);
     }
     ub += UNR * NT;
   }
-  for (; ub < u1; ub += NT) {  // the rest, bounds-checked
+  for (; ub < u1; ub += NT) {  // the rest, bounds-checked (fetch reads every row of the unit)
     typename Src::Raw raw;
     src.fetch(ub, raw);
-    uint4 w[EPU / 4];
-    unit_words<Src>(rk, ub, rid, j, tag, w);
-    race_take(src, raw, w, ub, a1, a2, best_u, &sm.tau);
+    race_take(src, raw, rk, rid, j, tag, ub, a1, a2, best_u, &sm.tau, true);
   }
   if (threadIdx.x == 0) sm.ncand = 0;
   const float A = __uint_as_float((uint32_t)block_max_u64<NT>(__float_as_uint(a1), sm.red));
@@ -581,21 +612,17 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
       }
     }
     __syncthreads();
-    // the listed candidate units, one element per lane
+    // the listed candidate units, one element per thread (kCandCap * EPU <= NT: one round, so
+    // the candidates' scattered loads are in flight together)
     const int nc = min(sm.ncand, kCandCap);
-    if (threadIdx.x < 32) {
-      for (int base = 0; base < nc * EPU; base += 32) {
-        const int l = base + (int)threadIdx.x;
-        if (l < nc * EPU) {
-          const uint32_t u = sm.cand[l / EPU];
-          const uint32_t x = u * EPU + (uint32_t)(l % EPU);
-          const float r = x < src.V ? src.at(x) : 0.0f;  // the last unit may pass the row end
-          if (r > 0.0f) {
-            const uint4 w4 = race_block(rk, x >> 2, rid, j, tag);
-            const uint64_t k = exact_key(r, word_of(w4, x & 3u), x);
-            best = k > best ? k : best;
-          }
-        }
+    for (int l = (int)threadIdx.x; l < nc * EPU; l += NT) {
+      const uint32_t u = sm.cand[l / EPU];
+      const uint32_t x = u * EPU + (uint32_t)(l % EPU);
+      const float r = x < src.V ? src.at(x) : 0.0f;  // the last unit may pass the row end
+      if (r > 0.0f) {
+        const uint4 w4 = race_block(rk, x >> 2, rid, j, tag);
+        const uint64_t k = exact_key(r, word_of(w4, x & 3u), x);
+        best = k > best ? k : best;
       }
     }
   }
@@ -742,19 +769,14 @@ __device__ uint64_t race_chunk_log(const uint16_t* row, uint32_t V, bool vec, fl
     }
     __syncthreads();
     const int nc = min(sm.ncand, kCandCap);
-    if (threadIdx.x < 32) {
-      for (int base = 0; base < nc * 8; base += 32) {
-        const int l = base + (int)threadIdx.x;
-        if (l < nc * 8) {
-          const uint32_t x = sm.cand[l / 8] * 8u + (uint32_t)(l % 8);
-          if (x < V) {
-            const float lv = bf16_bits_to_float(__ldg(row + x));
-            if (lv > -INFINITY) {
-              const uint4 w4 = race_block(rk, x >> 2, rid, j, tag);
-              const uint64_t k = log_exact_key(lv, c, word_of(w4, x & 3u), x);
-              best = k > best ? k : best;
-            }
-          }
+    for (int l = (int)threadIdx.x; l < nc * 8; l += NT) {  // one element per thread
+      const uint32_t x = sm.cand[l / 8] * 8u + (uint32_t)(l % 8);
+      if (x < V) {
+        const float lv = bf16_bits_to_float(__ldg(row + x));
+        if (lv > -INFINITY) {
+          const uint4 w4 = race_block(rk, x >> 2, rid, j, tag);
+          const uint64_t k = log_exact_key(lv, c, word_of(w4, x & 3u), x);
+          best = k > best ? k : best;
         }
       }
     }
@@ -1083,7 +1105,7 @@ __device__ void row_max2(const uint16_t* trow, const uint16_t* drow, uint32_t V,
 // The race on a logit row pair (HAS_Q) or on p alone, over the cluster: out of line, so that its
 // registers do not add to the statistics loop's.
 template <bool HAS_Q>
-__device__ __noinline__ uint64_t logit_race(const uint16_t* t, const uint16_t* d, float nrct,
+__device__ __forceinline__ uint64_t logit_race(const uint16_t* t, const uint16_t* d, float nrct,
                                             float invSt, float nrcd, float invSd, float c,
                                             uint32_t V, bool vec, uint32_t u0, uint32_t u1,
                                             const PhiloxRoundKeys& rk, uint32_t rid, uint32_t j,
@@ -1645,8 +1667,13 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
         if (valid) {
           Pv = __fdiv_rn(logit_term(ref_t(j), c, nrct), S.x);
           Qv = __fdiv_rn(logit_term(ref_d(j), c, nrcd), S.y);
-          const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
-          accept = u * (double)Qv < (double)Pv;
+          // the exact double test in one lane per warp (GB300's FP64 rate is low), shared
+          int acc = 0;
+          if ((threadIdx.x & 31) == 0) {
+            const double u = accept_uniform(P.rk, P.rbase + (uint32_t)r, (uint32_t)j);
+            acc = u * (double)Qv < (double)Pv;
+          }
+          accept = __shfl_sync(0xffffffffu, acc, 0) != 0;
         } else {
           e |= SD_ERR_TOKEN_RANGE;
         }
