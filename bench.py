@@ -480,12 +480,16 @@ def measure(name, args, sd, device, rank, world, steps, keep_set0=False):
     ms_per_step = total_ms / K
     value = shard.whole_job_rate(B * K, world, total_ms)
     bytes_v = float(np.mean([per_set[s % nsets][0] for s in range(CHUNK)]))
-    bytes_all = float(np.mean([sum(per_set[s % nsets][:3]) for s in range(CHUNK)]))
     bytes_read = float(np.mean([per_set[s % nsets][4] for s in range(CHUNK)]))
+    # the rebuild's and the gather's bytes, and the step's: verify counted by the rows it must read
+    bytes_rest = float(np.mean([sum(per_set[s % nsets][1:3]) for s in range(CHUNK)]))
+    bytes_all = bytes_read + bytes_rest
     peak, peak_kind = _peaks()
     # roofline of the dominant kernel: the fused step kernel moves the verify's, the expand's and
-    # the gather's bytes; the verify kernel alone the verify's
-    bytes_dom = bytes_all if fused else bytes_v
+    # the gather's bytes; the verify kernel alone the rows it must read (for probability rows the
+    # minimum-bytes model; for logit rows the rows up to the first rejection, the least any exact
+    # verify reads; the full-row model of every logit row is reported beside it)
+    bytes_dom = bytes_all if fused else bytes_read
     avg_dom = avg_f if fused else avg_v
     achieved = bytes_dom / (avg_dom * 1e-3) / 1e9
     traffic, traffic_note = (None, "no capture of the current kernel source")
@@ -507,16 +511,23 @@ def measure(name, args, sd, device, rank, world, steps, keep_set0=False):
         "algorithmic_bytes_per_launch": bytes_dom,
         "bytes_model": ("minimum bytes (scalar gathers + one p and one q row per sampled request, "
                         "a_r + 1 rows per greedy one)" if not logits else
-                        "full rows (2K + 1 logit rows per request)")
+                        "rows up to the first rejection (a_r + 1 target and min(a_r + 1, K) draft "
+                        "logit rows per request) + scalars")
         + ("; plus the rebuild's slots and hidden rows" if fused else ""),
-        "verify_alone": {"us": avg_v * 1e3, "bytes": bytes_v,
-                         "frac": bytes_v / (avg_v * 1e-3) / 1e9 / peak},
+        "verify_alone": {"us": avg_v * 1e3, "bytes": bytes_read,
+                         "frac": bytes_read / (avg_v * 1e-3) / 1e9 / peak},
         # the verify kernel against the bytes it must read (rows up to the first rejection):
         # its own efficiency, whatever the roofline model of the variant
         "frac_rows_read": (bytes_read / (avg_v * 1e-3) / 1e9) / peak,
         "rows_read_bytes": bytes_read,
         "step_frac": (bytes_all / (ms_per_step * 1e-3) / 1e9) / peak,
     }
+    if logits:
+        # the full-row model (every target and draft logit row of every request, 2K + 1 rows):
+        # bytes no lazy verify reads, so this fraction can exceed 1
+        roofline["full_row"] = {"bytes": bytes_v, "frac": bytes_v / (avg_v * 1e-3) / 1e9 / peak,
+                                "step_frac": (bytes_v + bytes_rest)
+                                / (ms_per_step * 1e-3) / 1e9 / peak}
     res = {
         "cfg": cfg, "B": B, "steps": K, "value": value, "ms_per_step": ms_per_step,
         "launches": step_kernels, "clocks": clk, "roofline": roofline,

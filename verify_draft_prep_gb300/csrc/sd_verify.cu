@@ -951,18 +951,29 @@ __device__ void argmax_chunk2(const void* row0, const void* row1, uint32_t V, bo
 constexpr float kRefSumLimit = 0x1p100f;
 constexpr int kLookAhead = 4;  // the next row's first 1/kLookAhead is streamed during the exchange
 
+// Compensated running sums, kept as two lanes (even and odd elements of each 32-bit word pair)
+// so that the scaling, the sums and the compensation run as packed fp32x2 instructions: half the
+// issue slots of the scalar forms, each lane rounded exactly as the scalar operation would be.
 struct RefAcc {
-  float s = 0.0f, comp = 0.0f;  // compensated running sum
+  float2 s = make_float2(0.0f, 0.0f), comp = make_float2(0.0f, 0.0f);
+  __device__ __forceinline__ float total() const { return (s.x - comp.x) + (s.y - comp.y); }
 };
 
 __device__ __forceinline__ void absorb_ref(RefAcc& a, const uint4& raw, float c, float nrc) {
-  float e[8];
+  const float2 c2 = make_float2(c, c), n2 = make_float2(nrc, nrc), m1 = make_float2(-1.0f, -1.0f);
+  const uint32_t v[4] = {raw.x, raw.y, raw.z, raw.w};
+  float2 e[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) e[i] = logit_term(bf16_at(raw, i), c, nrc);
-  const float part = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-  const float y = part - a.comp;
-  const float t = a.s + y;
-  a.comp = (t - a.s) - y;
+  for (int i = 0; i < 4; ++i) {
+    // elements 2i (low half) and 2i+1 (high half): l c + nrc, as logit_term rounds it
+    const float2 l = make_float2(__uint_as_float(v[i] << 16), __uint_as_float(v[i] & 0xffff0000u));
+    const float2 y = __ffma2_rn(l, c2, n2);
+    e[i] = make_float2(fast_ex2(y.x), fast_ex2(y.y));
+  }
+  const float2 part = __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
+  const float2 y = __ffma2_rn(a.comp, m1, part);               // part - comp
+  const float2 t = __fadd2_rn(a.s, y);
+  a.comp = __ffma2_rn(y, m1, __ffma2_rn(a.s, m1, t));          // (t - s) - y
   a.s = t;
 }
 
@@ -1127,7 +1138,7 @@ __device__ __noinline__ float2 logit_row_refit(const uint16_t* trow, const uint1
   RefAcc ft, fd;
   if (drow) ref_sums<true>(trow, drow, V, vec, u0, u1, c, nrct, nrcd, ft, fd);
   else ref_sums<false>(trow, nullptr, V, vec, u0, u1, c, nrct, 0.0f, ft, fd);
-  const float2 fm = block_sum2(ft.s - ft.comp, fd.s - fd.comp, sm, par);
+  const float2 fm = block_sum2(ft.total(), fd.total(), sm, par);
   cluster_post(fm, &sm.xslot_fb, cl);
   return cluster_collect(fm, &sm.xslot_fb, cl);
 }
@@ -1646,7 +1657,7 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
     };
     RefAcc at, ad;
     stream(0, u0, u1, at, ad);
-    float2 mine = block_sum2(at.s - at.comp, ad.s - ad.comp, sm, par);
+    float2 mine = block_sum2(at.total(), ad.total(), sm, par);
     cluster_post(mine, &sm.xslot[0], cl);
     for (int j = 0;; ++j) {
       // look-ahead: the first units of row j+1 while the cluster's sums of row j arrive
@@ -1706,7 +1717,7 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
       }
       // accepted: the rest of row j+1, then its sums go to the cluster
       stream(j + 1, us, u1, nt, nd);
-      mine = block_sum2(nt.s - nt.comp, nd.s - nd.comp, sm, par);
+      mine = block_sum2(nt.total(), nd.total(), sm, par);
       cluster_post(mine, &sm.xslot[(j + 1) & 1], cl);
     }
   }
