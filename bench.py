@@ -56,6 +56,19 @@ def _src_hash():
     return h.hexdigest()[:16]
 
 
+def philox_peak():
+    """Philox4x32-10 blocks per second the GPU's integer multipliers allow, from unit counts and
+    the clock: each block takes 20 32x32->64-bit products (two per round), each product two
+    operations of an SM's 64 integer-multiply lanes per clock; 152 SMs at the maximum SM clock
+    (MEASURED_PEAKS.json, else 2070 MHz)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    return 152 * mhz * 1e6 * 64 / (20 * 2)
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -151,6 +164,27 @@ def algorithmic_bytes(w, a):
     gather = int(((a + 1) * 2 * H + (a + K) * 2 * H).sum()) + 2 * H
     del torch
     return verify, expand, gather, verify_read
+
+
+def sample_roofline(w, avg_ms, sample_bytes, peak):
+    """The drafter-side sampler against both of its bounds: HBM (every row read once) and the
+    integer multipliers (one Philox4x32-10 block per 4 entries of every sampled row, the race's
+    variates). The binding one is the bound whose time is longer."""
+    rows = w.B * w.K
+    blocks = rows * ((w.V + 3) // 4)
+    pk_alu = philox_peak()
+    t_hbm, t_alu = sample_bytes / (peak * 1e9), blocks / pk_alu
+    hbm = {"achieved_GBps": sample_bytes / (avg_ms * 1e-3) / 1e9,
+           "frac": sample_bytes / (avg_ms * 1e-3) / 1e9 / peak}
+    alu = {"philox_blocks_per_launch": blocks,
+           "achieved_blocks_per_s": blocks / (avg_ms * 1e-3), "peak_blocks_per_s": pk_alu,
+           "frac": blocks / (avg_ms * 1e-3) / pk_alu,
+           "peak_source": "unit counts: 152 SMs x max SM clock x 64 multiply lanes / 40 lane "
+                          "operations per block"}
+    bound = "alu" if t_alu > t_hbm else "hbm"
+    return {"kernel": "sd_draft_sample", "us": avg_ms * 1e3, "bound": bound,
+            "frac": (alu if bound == "alu" else hbm)["frac"], "bytes_per_launch": sample_bytes,
+            "achieved_GBps": hbm["achieved_GBps"], "hbm_frac": hbm["frac"], "alu": alu}
 
 
 def make_set(cfg_name, s, device, rank, batch=None):
@@ -533,12 +567,9 @@ def measure(name, args, sd, device, rank, world, steps, keep_set0=False):
         "launches": step_kernels, "clocks": clk, "roofline": roofline,
         "config": config_dict(cfg, B, nsets, rows_gb, world, batch),
         "dtype": "f32" if not logits else "bf16",
-        "draft_sample": {"kernel": "sd_draft_sample", "us": avg_s * 1e3,
-                         "bytes_per_launch": sample_bytes,
-                         "achieved_GBps": sample_bytes / (avg_s * 1e-3) / 1e9,
-                         "frac": sample_bytes / (avg_s * 1e-3) / 1e9 / peak,
-                         "rows": f"B*K = {w0s.B * w0s.K} rows of V = {w0s.V}, each read once "
-                                 "from HBM"},
+        "draft_sample": dict(sample_roofline(w0s, avg_s, sample_bytes, peak),
+                             rows=f"B*K = {w0s.B * w0s.K} rows of V = {w0s.V}, each read once "
+                                  "from HBM"),
         "prepare_padded": {"kernel": "sd_pdraft_prepare_padded", "us": avg_pp * 1e3,
                            "bytes_per_launch": pad_bytes,
                            "achieved_GBps": pad_bytes / (avg_pp * 1e-3) / 1e9,

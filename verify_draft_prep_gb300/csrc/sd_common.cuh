@@ -60,14 +60,15 @@ inline PhiloxRoundKeys philox_round_keys(uint64_t seed) {
   return rk;
 }
 
+// Each round's two products as full 64-bit results (one wide multiply each, high and low halves
+// together): fewer issue slots than separate high and low multiplies, the same words.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxRoundKeys& rk) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ rk.k0[i], lo1, hi0 ^ c.w ^ rk.k1[i], lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk.k0[i], (uint32_t)p1,
+                   (uint32_t)(p0 >> 32) ^ c.w ^ rk.k1[i], (uint32_t)p0);
   }
   return c;
 }

@@ -2181,7 +2181,7 @@ extern "C" int sd_verify_noalloc_launch(int B, int K, int V, int dtype, const vo
                           q_at_draft, slots, err, stream);
 }
 
-// Drafter-side sampling: one cluster per row (the verify kernel's cluster size for V).
+// Drafter-side sampling: one cluster per row.
 extern "C" int sd_sample_launch(int B, int K, int V, int dtype, const void* rows, long ld,
                                 const float* temperature, uint64_t seed, uint32_t request_base,
                                 int32_t* drafts, int32_t* err, cudaStream_t stream) {
@@ -2199,7 +2199,12 @@ extern "C" int sd_sample_launch(int B, int K, int V, int dtype, const void* rows
   P.rbase = request_base;
   P.drafts = drafts;
   P.err = err;
+  // CTAs per row: as few as still give the launch about 1.5 waves of kMinBlocksF32 CTAs per SM
+  // (a row's CTAs meet at a cluster barrier and share the candidate pass; more rows per wave
+  // amortise both), no more than the row splits into
   P.cl = choose_cluster(V, epu);
+  const long rows_n = (long)B * K, want = 3L * sdk::kMinBlocksF32 * sm_count() / 2;
+  while (P.cl > 1 && rows_n * (P.cl / 2) >= want) P.cl >>= 1;
   P.vec = ((uintptr_t)rows % 16 == 0) && ((ld * esize) % 16 == 0);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * K * P.cl), 1, 1);
