@@ -40,11 +40,11 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "df83d055a48aba31"): (85.738752e6, "ncu --set full, one fused launch of the full "
+    ("b64", "16dd15643501bf27"): (90.780672e6, "ncu --set full, one fused launch of the full "
                                                "batch (one input set)"),
-    ("b256mix", "df83d055a48aba31"): (439.708672e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "df83d055a48aba31"): (776.221355e6, "ncu --set full at B=192, scaled x512/192"),
-    ("b1024lg", "df83d055a48aba31"): (3097.54539e6, "ncu --set full at B=96, scaled x1024/96"),
+    ("b256mix", "16dd15643501bf27"): (434.404352e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "16dd15643501bf27"): (784.758101e6, "ncu --set full at B=192, scaled x512/192"),
+    ("b1024lg", "16dd15643501bf27"): (3708.917077e6, "ncu --set full at B=96, scaled x1024/96"),
 }
 
 
