@@ -86,3 +86,26 @@ def test_reference_arm_prints_the_timed_arms_config(capsys):
     assert set(line["config"]) == set(bench.config_dict(cfg, 1, 4, 0.0, 1, 0))
     assert line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+
+
+def test_philox_peak_from_unit_counts():
+    # 152 SMs x clock x 64 multiply lanes, 40 lane operations (20 64-bit products) per block
+    assert abs(bench.philox_peak() - 152 * 2070e6 * 64 / 40) / bench.philox_peak() < 0.05
+
+
+def test_sampler_roofline_binds_on_the_longer_bound():
+    import types
+    peak = 6753.8
+    # bf16 rows of 2e5 entries: one Philox block per 4 entries outweighs 2 bytes per entry
+    w = types.SimpleNamespace(B=1024, K=8, V=201088)
+    by = w.B * w.K * w.V * 2
+    r = bench.sample_roofline(w, 1.2, by, peak)
+    assert r["bound"] == "alu" and r["frac"] == r["alu"]["frac"]
+    blocks = w.B * w.K * ((w.V + 3) // 4)
+    assert r["alu"]["philox_blocks_per_launch"] == blocks
+    assert abs(r["alu"]["frac"] - blocks / 1.2e-3 / bench.philox_peak()) < 1e-12
+    assert abs(r["hbm_frac"] - by / 1.2e-3 / 1e9 / peak) < 1e-12
+    # fp32 rows: 4 bytes per entry at the copy bandwidth take longer than the Philox work
+    w = types.SimpleNamespace(B=64, K=5, V=201088)
+    r = bench.sample_roofline(w, 0.075, w.B * w.K * w.V * 4, peak)
+    assert r["bound"] == "hbm" and r["frac"] == r["hbm_frac"]
