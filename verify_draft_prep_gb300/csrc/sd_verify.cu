@@ -369,6 +369,7 @@ struct Smem {
   uint32_t cand[kCandCap];
   int last;
   uint32_t tau;  // race_take's running best of the current race_chunk call (fp32 bits)
+  uint64_t race_best;  // race_chunk's exact maximum over the CTA
 };
 
 // Cluster-wide maximum of a CTA-uniform value. Every CTA of the cluster calls it the same
@@ -582,9 +583,14 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
     src.fetch(ub, raw);
     race_take(src, raw, rk, rid, j, tag, ub, a1, a2, best_u, &sm.tau, true);
   }
-  if (threadIdx.x == 0) sm.ncand = 0;
-  const float A = __uint_as_float((uint32_t)block_max_u64<NT>(__float_as_uint(a1), sm.red));
-  if (threadIdx.x == 0) sm.tau = 0u;  // every thread has left the streaming pass
+  if (threadIdx.x == 0) {
+    sm.ncand = 0;
+    sm.race_best = 0ull;
+  }
+  // A, the CTA's largest unit maximum, is in tau once every thread has left the streaming pass:
+  // a unit maximum not posted there was at most the value tau held when the thread read it
+  __syncthreads();
+  const float A = __uint_as_float(*(volatile uint32_t*)&sm.tau);
   uint64_t best = 0ull;
   if (A > 0.0f) {
     // A CTA maximum below about 2^-100 in key units: fp32 keys are near the subnormal range
@@ -612,6 +618,7 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
       }
     }
     __syncthreads();
+    if (threadIdx.x == 0) sm.tau = 0u;  // every thread has read A
     // the listed candidate units, one element per thread (kCandCap * EPU <= NT: one round, so
     // the candidates' scattered loads are in flight together)
     const int nc = min(sm.ncand, kCandCap);
@@ -625,8 +632,22 @@ __device__ __forceinline__ uint64_t race_chunk(const Src& src, uint32_t u0, uint
         best = k > best ? k : best;
       }
     }
+  } else {
+    __syncthreads();
+    if (threadIdx.x == 0) sm.tau = 0u;  // every thread has read A
   }
-  return block_max_u64<NT>(best, sm.red);
+  // the CTA's best exact key: warp maxima into one shared 64-bit maximum
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+    best = other > best ? other : best;
+  }
+  if ((threadIdx.x & 31) == 0 && best)
+    atomicMax((unsigned long long*)&sm.race_best, (unsigned long long)best);
+  __syncthreads();
+  const uint64_t m = sm.race_best;
+  __syncthreads();  // every thread has read it before the next call resets it
+  return m;
 }
 
 // ------------------------------------------------------------- log-domain race on logit rows
