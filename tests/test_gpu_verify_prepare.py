@@ -134,6 +134,39 @@ def test_error_paths_match_the_two_calls():
         assert err & sd.SD_ERR_BLOCK_TABLE and err & sd.SD_ERR_TOTAL_RANGE
 
 
+@pytest.mark.parametrize("B,greedy_every", [(48, 0), (40, 3), (1024, 0)])
+def test_logit_rows_same_bytes_as_the_two_calls(B, greedy_every):
+    # logit rows: the verify kernel (softmax statistics, decisions and races), then the rebuild
+    # kernel; every output, greedy requests among them, against the two calls
+    w = workloads.make("b1024lg", device="cuda", B=B)
+    T = w.temperature.clone()
+    if greedy_every:
+        T[::greedy_every] = 0.0
+    assert sd.sd_verify_prepare_kernels(w.B, w.K, w.V, sd.SD_BF16_LOGITS, True) == 2
+    ws = new_ws(w.B)
+    want = run_separate(w, T, w.capacity)
+    for _ in range(2):  # the workspace comes back zeroed and serves the next call
+        got = run_fused(w, T, w.capacity, ws)
+        assert_same(got, want)
+        assert int(ws.count_nonzero()) == 0
+    assert int(got["err"].item()) == 0
+    assert int((got["input_ids"] == -1).sum()) == w.capacity - int(got["total_out"].item())
+
+
+def test_logit_rows_error_paths_match_the_two_calls():
+    w = workloads.make("b1024lg", device="cuda", B=24)
+    table = w.block_table.clone()
+    table[5, :] = -1                      # request 5's slots miss the table
+    n_in = w.B * (w.K + 1) - 7            # the last request's late hidden rows are missing
+    hidden = w.hidden[:n_in]
+    cap = w.B * w.K                       # too small for every outcome
+    want = run_separate(w, w.temperature, cap, hidden=hidden, table=table)
+    got = run_fused(w, w.temperature, cap, new_ws(w.B), hidden=hidden, table=table)
+    assert_same(got, want)
+    err = int(got["err"].item())
+    assert err & sd.SD_ERR_BLOCK_TABLE and err & sd.SD_ERR_TOTAL_RANGE
+
+
 def test_out_of_range_drafts_match_the_two_calls():
     # a draft token outside [0, V) is rejected with SD_ERR_TOKEN_RANGE; on the single launch the
     # rebuild CTA, which recomputes the decisions, raises it
