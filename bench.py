@@ -40,11 +40,11 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "16dd15643501bf27"): (90.780672e6, "ncu --set full, one fused launch of the full "
+    ("b64", "c81fb81db8351602"): (90.737152e6, "ncu --set full, one fused launch of the full "
                                                "batch (one input set)"),
-    ("b256mix", "16dd15643501bf27"): (434.404352e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "16dd15643501bf27"): (784.758101e6, "ncu --set full at B=192, scaled x512/192"),
-    ("b1024lg", "16dd15643501bf27"): (3708.917077e6, "ncu --set full at B=96, scaled x1024/96"),
+    ("b256mix", "c81fb81db8351602"): (434.83392e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "c81fb81db8351602"): (785.671509e6, "ncu --set full at B=192, scaled x512/192"),
+    ("b1024lg", "c81fb81db8351602"): (3702.97242e6, "ncu --set full at B=96, scaled x1024/96"),
 }
 
 
