@@ -271,6 +271,19 @@ def launch_prepare_padded(sd, w, o, stream=None):
                                 stream=stream)
 
 
+def launch_verify_prepare_padded(sd, w, o, stream=None):
+    """The step with the padded drafter batch in one call (one launch for an all-sampled batch
+    of one wave)."""
+    sd.sd_verify_prepare_padded(w.target, w.draft, w.drafts, o["out_tokens"], o["num_accepted"],
+                                w.pos0, w.block_table, w.block_size, w.mask_token_id,
+                                o["pad_ids"], o["pad_pos"], o["pad_slot"], o["pad_map"],
+                                o["pad_masked"], o["pad_rej"], o["pad_scatter"], o["pad_nti"],
+                                target_hidden=w.hidden, h_shared=w.h_shared,
+                                out_hidden=o["pad_hidden"], temperature=temperatures(w),
+                                seed=w.seed, err=o["err"], stream=stream, workspace_buf=o["ws"],
+                                request_base=getattr(w, "request_base", 0))
+
+
 def time_graph(fn, sets, outs, stream, K):
     """Average duration (ms) of K launches of `fn`, rotating over the input sets, replayed
     from one CUDA graph."""
@@ -502,6 +515,9 @@ def measure(name, args, sd, device, rank, world, steps, keep_set0=False):
     # the padded form of the rebuild (fixed 2K-slot rows), timed alone after the same verify
     avg_pp = time_graph(lambda w, o, st: launch_prepare_padded(sd, w, o, st), sets, outs, stream,
                         CHUNK)
+    # ... and the whole step with the padded batch through the one call
+    avg_vpp = time_graph(lambda w, o, st: launch_verify_prepare_padded(sd, w, o, st), sets, outs,
+                         stream, CHUNK)
     # the next row of the method: drafter-side sampling of the K new drafts, timed alone
     avg_s = time_graph(lambda w, o, st: launch_draft_sample(sd, w, o, st), sets, outs, stream,
                        CHUNK)
@@ -576,7 +592,15 @@ def measure(name, args, sd, device, rank, world, steps, keep_set0=False):
                            "frac": pad_bytes / (avg_pp * 1e-3) / 1e9 / peak,
                            "rows": f"B*2K = {w0s.B * 2 * w0s.K} drafter rows, every one written "
                                    "(hidden states read for the a_r + 1 target rows of each "
-                                   "request)"},
+                                   "request)",
+                           # the step with this batch in one call (sd_verify_prepare_padded):
+                           # the verify's bytes and the padded rebuild's
+                           "step_one_call": {
+                               "us": avg_vpp * 1e3,
+                               "two_calls_us": (avg_v + avg_pp) * 1e3,
+                               "launches": sd.sd_verify_prepare_kernels(
+                                   w0s.B, w0s.K, w0s.V, dt_code, has_t),
+                               "frac": (bytes_read + pad_bytes) / (avg_vpp * 1e-3) / 1e9 / peak}},
         "info": {"verify_ms": avg_v, "prepare_ms": avg_p,
                  "step_ms_median": float(np.median(step_ms)) if step_ms else None,
                  "step_bytes": bytes_all,

@@ -396,6 +396,36 @@ SD_API int sd_pdraft_prepare_padded(int B, int K, const int32_t* out_tokens,
                                     void* out_hidden, long ld_out, int32_t* err, void* stream);
 
 /*
+ * sd_verify_prepare_padded -- sd_verify then sd_pdraft_prepare_padded in one call.
+ *
+ * The step of sd_verify_prepare with the drafter batch in the fixed-width layout of
+ * sd_pdraft_prepare_padded (P-EAGLE blog, "Hidden State 管理": rejected tokens on
+ * PADDING_SLOT_ID, target hidden states scattered to their drafter rows). When every request
+ * samples on probability rows (temperature NULL) and the batch fits one wave (the conditions of
+ * sd_verify_prepare's single launch), this is one launch: CTA r (r < B) recomputes request r's
+ * accept decisions from the inputs -- in this layout no request's rows depend on another's counts
+ * -- and writes all 2K rows of request r but the token at row r*2K + a_r, which the CTA that
+ * completes the request's race writes; nothing waits. Other batches run the verify kernel and
+ * then the padded rebuild kernel. Either way every output is bit for bit what sd_verify then
+ * sd_pdraft_prepare_padded write; sd_verify_prepare_kernels gives the number of launches.
+ *
+ * Arguments: sd_verify's (workspace of at least sd_verify_workspace_bytes(B, K, V, dtype),
+ * 16-byte aligned, zeroed before first use and left zeroed by every call) then
+ * sd_pdraft_prepare_padded's from pos0 on (out_tokens and num_accepted are this call's own
+ * outputs). Errors: those of both calls.
+ */
+SD_API int sd_verify_prepare_padded(
+    int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
+    const int32_t* drafts, const float* temperature, uint64_t seed, uint32_t request_base,
+    int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+    const int32_t* pos0, const int32_t* block_table, int max_blocks, int block_size,
+    int32_t mask_token_id, int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
+    int32_t* hidden_map, uint8_t* is_masked, uint8_t* rejected, int32_t* scatter_map,
+    int32_t* new_token_idx, int H, const void* target_hidden, long ld_in, int n_in_rows,
+    const void* h_shared, void* out_hidden, long ld_out, void* workspace, size_t workspace_bytes,
+    int32_t* err, void* stream);
+
+/*
  * sd_hidden_gather -- drafter hidden states.
  *
  * P-EAGLE blog (vLLM), section "Hidden State 管理": target hidden states are copied to their

@@ -36,7 +36,8 @@ EXPORTED = ["sd_verify", "sd_verify_workspace_bytes", "sd_verify_kernels",
             "sd_verify_ragged", "sd_pdraft_prepare_ragged", "sd_pdraft_expand", "sd_pdraft_prepare", "sd_hidden_gather", "sd_philox_words", "sd_race_E",
             "sd_race_E_approx_error", "sd_race_E_check", "sd_status_string", "sd_version",
             "sd_verify_prepare", "sd_verify_prepare_workspace_bytes", "sd_verify_prepare_kernels",
-            "sd_verify_prepare_ragged", "sd_diag_verify_prepare_withheld"]
+            "sd_verify_prepare_ragged", "sd_diag_verify_prepare_withheld",
+            "sd_verify_prepare_padded"]
 
 _lock = threading.Lock()
 _lib = None
@@ -103,6 +104,11 @@ def load():
                                                  P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P,
                                                  i64, P, P]
         lib.sd_pdraft_prepare_padded.restype = i32
+        lib.sd_verify_prepare_padded.argtypes = [i32, i32, i32, i32, P, i64, P, i64, P, P, u64,
+                                                 u32, P, P, P, P, P, P, i32, i32, ctypes.c_int32,
+                                                 P, P, P, P, P, P, P, P, i32, P, i64, i32, P, P,
+                                                 i64, P, ctypes.c_size_t, P, P]
+        lib.sd_verify_prepare_padded.restype = i32
         lib.sd_hidden_gather.argtypes = [i32, i32, P, P, P, i64, i32, P, P, i64, P, P]
         lib.sd_hidden_gather.restype = i32
         lib.sd_philox_words.argtypes = [i32, P, u64, P, P]
@@ -439,6 +445,47 @@ def sd_pdraft_prepare_padded(out_tokens, num_accepted, pos0, block_table, block_
         _ptr(out_hidden), _row_stride(out_hidden) if out_hidden is not None else H, _ptr(err),
         _stream(input_ids, stream))
     _check(rc, "sd_pdraft_prepare_padded")
+
+
+def sd_verify_prepare_padded(target, draft, drafts, out_tokens, num_accepted, pos0, block_table,
+                             block_size, mask_token_id, input_ids, positions, slot_mapping,
+                             hidden_map, is_masked, rejected, scatter_map, new_token_idx,
+                             target_hidden=None, h_shared=None, out_hidden=None, temperature=None,
+                             seed=0, p_at_draft=None, q_at_draft=None, err=None, stream=None,
+                             workspace_buf=None, request_base=0):
+    """sd_verify then sd_pdraft_prepare_padded on its outputs, in one call (see include/sd.h):
+    arguments as for the two calls; workspace_buf as for sd_verify."""
+    import torch
+
+    B, K = drafts.shape
+    V = target.shape[1]
+    if target.dtype == torch.float32:
+        dtype = SD_F32_PROBS
+    elif target.dtype == torch.bfloat16:
+        dtype = SD_BF16_LOGITS
+    else:
+        raise SDError("target must be float32 probabilities or bfloat16 logits")
+    if draft.dtype != target.dtype or draft.shape[1] != V:
+        raise SDError("draft must match target's dtype and vocabulary")
+    if target.shape[0] != B * (K + 1) or draft.shape[0] != B * K:
+        raise SDError("row counts must be B*(K+1) (target) and B*K (draft)")
+    if input_ids.shape[0] != B * 2 * K:
+        raise SDError("padded outputs have B*2K entries")
+    H = out_hidden.shape[1] if out_hidden is not None else 1
+    n_in = target_hidden.shape[0] if target_hidden is not None else 0
+    ws = workspace_buf if workspace_buf is not None else workspace(_device(target), B, K, V,
+                                                                   dtype)
+    rc = load().sd_verify_prepare_padded(
+        B, K, V, dtype, _ptr(target), _row_stride(target), _ptr(draft), _row_stride(draft),
+        _ptr(drafts), _ptr(temperature), seed, request_base, _ptr(out_tokens),
+        _ptr(num_accepted), _ptr(p_at_draft), _ptr(q_at_draft), _ptr(pos0), _ptr(block_table),
+        block_table.shape[1], block_size, mask_token_id, _ptr(input_ids), _ptr(positions),
+        _ptr(slot_mapping), _ptr(hidden_map), _ptr(is_masked), _ptr(rejected), _ptr(scatter_map),
+        _ptr(new_token_idx), H, _ptr(target_hidden),
+        _row_stride(target_hidden) if target_hidden is not None else H, n_in, _ptr(h_shared),
+        _ptr(out_hidden), _row_stride(out_hidden) if out_hidden is not None else H, _ptr(ws),
+        ws.numel(), _ptr(err), _stream(target, stream))
+    _check(rc, "sd_verify_prepare_padded")
 
 
 def sd_hidden_gather(total_out, hidden_map, target_hidden, h_shared, out_hidden, err=None,

@@ -47,6 +47,12 @@ int sd_verify_prepare_withheld_launch(int, uint32_t, int, int, int, int, const v
                                       const void*, long, int, const void*, void*, long, void*,
                                       int32_t*, cudaStream_t);
 int sd_verify_prepare_kernel_count(int, int, int, int, int);
+int sd_verify_prepare_padded_launch(int, int, int, int, const void*, long, const void*, long,
+                                    const int32_t*, const float*, uint64_t, uint32_t, int32_t*,
+                                    int32_t*, float*, float*, const int32_t*, const int32_t*, int,
+                                    int, int32_t, int32_t*, int32_t*, int32_t*, int32_t*,
+                                    uint8_t*, uint8_t*, int32_t*, int32_t*, int, const void*, long,
+                                    int, const void*, void*, long, void*, int32_t*, cudaStream_t);
 }
 
 namespace {
@@ -519,6 +525,52 @@ int sd_verify_prepare_ragged(int B, int K_max, int V, int dtype, const void* tar
                         is_rejected, start_loc, new_token_idx, total_out, H, target_hidden,
                         ld_in, n_in_rows, h_shared, out_hidden, ld_out, workspace,
                         workspace_bytes, err, stream);
+}
+
+int sd_verify_prepare_padded(int B, int K, int V, int dtype, const void* target, long ld_t,
+                             const void* draft, long ld_d, const int32_t* drafts,
+                             const float* temperature, uint64_t seed, uint32_t request_base,
+                             int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft,
+                             float* q_at_draft, const int32_t* pos0, const int32_t* block_table,
+                             int max_blocks, int block_size, int32_t mask_token_id,
+                             int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
+                             int32_t* hidden_map, uint8_t* is_masked, uint8_t* rejected,
+                             int32_t* scatter_map, int32_t* new_token_idx, int H,
+                             const void* target_hidden, long ld_in, int n_in_rows,
+                             const void* h_shared, void* out_hidden, long ld_out,
+                             void* workspace, size_t workspace_bytes, int32_t* err, void* stream) {
+  // sd_verify's checks
+  if (dtype != SD_F32_PROBS && dtype != SD_BF16_LOGITS) return SD_E_DTYPE;
+  if (B < 0 || K < 1 || K > SD_K_MAX || V < 1 || ld_t < V || ld_d < V) return SD_E_SHAPE;
+  if ((long long)B * (K + 1) > 2147483647LL) return SD_E_SHAPE;
+  if ((unsigned long long)request_base + (unsigned long long)B > 4294967296ULL) return SD_E_SHAPE;
+  // sd_pdraft_prepare_padded's checks
+  if (max_blocks < 0 || block_size < 1) return SD_E_SHAPE;
+  if ((long long)B * 2 * K > 2147483647LL) return SD_E_SHAPE;
+  if (B == 0) return SD_OK;
+  if (!out_tokens || !num_accepted || !pos0 || (max_blocks > 0 && !block_table) || !input_ids ||
+      !positions || !slot_mapping || !hidden_map || !is_masked || !rejected || !scatter_map ||
+      !new_token_idx)
+    return SD_E_NULL;
+  if (out_hidden) {
+    if (H < 1 || ld_in < H || ld_out < H || n_in_rows < 0) return SD_E_SHAPE;
+    if (!h_shared || (n_in_rows > 0 && !target_hidden)) return SD_E_NULL;
+    if ((uintptr_t)target_hidden % 2 || (uintptr_t)h_shared % 2 || (uintptr_t)out_hidden % 2)
+      return SD_E_ALIGN;
+  }
+  if (!target || !draft || !drafts || !workspace) return SD_E_NULL;
+  if (workspace_bytes < sd_verify_workspace_bytes(B, K, V, dtype)) return SD_E_SHAPE;
+  const int esize = dtype == SD_F32_PROBS ? 4 : 2;
+  if ((uintptr_t)target % esize || (uintptr_t)draft % esize) return SD_E_ALIGN;
+  if ((uintptr_t)workspace % 16) return SD_E_ALIGN;
+  const int rc = check_device();
+  if (rc != SD_OK) return rc;
+  return sd_verify_prepare_padded_launch(
+      B, K, V, dtype, target, ld_t, draft, ld_d, drafts, temperature, seed, request_base,
+      out_tokens, num_accepted, p_at_draft, q_at_draft, pos0, block_table, max_blocks, block_size,
+      mask_token_id, input_ids, positions, slot_mapping, hidden_map, is_masked, rejected,
+      scatter_map, new_token_idx, H, target_hidden, ld_in, n_in_rows, h_shared, out_hidden,
+      ld_out, workspace, err, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -107,6 +107,11 @@ struct RebuildArgs {
   uint16_t* out_hidden;  // nullptr: metadata only
   long ld_out;
   int hvec;              // 16-byte aligned hidden rows, H a multiple of 8
+  // the padded layout (sd_verify_prepare_padded): fixed 2K-slot rows, per-slot rejected mask
+  // and the scatter form of the hidden map; capacity, start_loc and total_out are unused
+  int padded;
+  uint8_t* rejected;
+  int32_t* scatter_map;
 };
 
 struct VerifyParams {
@@ -133,7 +138,7 @@ struct VerifyParams {
                        // request in the cluster role)
   int vec;  // 1: every row starts on a 16-byte boundary
   int fuse;  // 1: CTAs [0, B) rebuild the drafter batch, CTAs [B, grid) race (spread over the
-             // requests as evenly as they go)
+             // requests as evenly as they go); 2: the same with the padded layout
   RebuildArgs rb;
   uint64_t wait_ns;  // bound of the completing race CTA's wait for the published slot
   int withhold;      // diagnostic (-1: none): this request's rebuild CTA publishes its slot only
@@ -1381,6 +1386,63 @@ __device__ __noinline__ void rebuild_role(const VerifyParams& P, int r, Smem& sm
   if (e) raise_err(P.err, e);
 }
 
+// The padded rebuild role of request r (sd_verify_prepare_padded, CTA r of the launch): request r
+// owns drafter rows [r*2K, (r+1)*2K) whatever the other requests accept, so the CTA needs only
+// its own request's accept decisions (recomputed from the inputs, all K at once) and writes every
+// row of the request -- the same bytes as the padded rebuild kernel -- except the token at row
+// r*2K + a_r, which the CTA that completes the request's race writes.
+__device__ __noinline__ void padded_rebuild_role(const VerifyParams& P, int r, Smem& sm) {
+  const RebuildArgs& R = P.rb;
+  const int K = P.K, W = 2 * K;
+  const ReqRows rr = req_rows(P, r);
+  if (threadIdx.x == 0) sm.a = K;
+  __syncthreads();
+  if (threadIdx.x < (unsigned)K) {
+    float Pv, Qv;
+    bool bad;
+    if (!draft_accepted(P, rr, r, (int)threadIdx.x, Pv, Qv, bad)) atomicMin(&sm.a, (int)threadIdx.x);
+  }
+  __syncthreads();
+  const int a = sm.a;
+  int32_t e = 0;
+  const int p0 = __ldg(R.pos0 + r);
+  const long long row0 = (long long)r * W;
+  for (int j = threadIdx.x; j < W; j += NT) {
+    const long long row = row0 + j;
+    const bool live = j < a + K;
+    const long long pos = (long long)p0 + 1 + j;
+    int32_t slot = -1;
+    if (live) {
+      const long long blk = pos >= 0 ? pos / R.block_size : -1;
+      if (blk < 0 || blk >= R.max_blocks) {
+        e |= SD_ERR_BLOCK_TABLE;
+      } else {
+        const long long phys = __ldg(R.block_table + (size_t)r * R.max_blocks + blk);
+        const long long sl = phys * R.block_size + pos % R.block_size;
+        if (phys < 0 || sl > 2147483647LL) e |= SD_ERR_BLOCK_TABLE;
+        else slot = (int32_t)sl;
+      }
+    }
+    // row a_r's token is the race's result: its CTA writes it
+    if (j < a) R.input_ids[row] = __ldg(P.drafts + rr.d0 + j);
+    else if (j > a) R.input_ids[row] = R.mask_id;
+    R.positions[row] = (int32_t)pos;
+    R.slot_mapping[row] = slot;
+    R.hidden_map[row] = (j <= a) ? (int32_t)(rr.t0 + j) : -1;
+    R.is_masked[row] = (live && j > a) ? 1 : 0;
+    R.rejected[row] = live ? 0 : 1;
+    if (j <= K) R.scatter_map[rr.t0 + j] = (j <= a) ? (int32_t)row : -1;
+    if (j < K) R.new_token_idx[(size_t)r * K + j] = (int32_t)(row0 + a + j);
+  }
+  if (R.out_hidden) {
+    for (int j = threadIdx.x >> 5; j < W; j += NT / 32)
+      gather_row_warp(j <= a ? (long long)rr.t0 + j : -1, R.hidden, R.ld_in, R.n_in_rows,
+                      R.h_shared, R.out_hidden + (row0 + j) * R.ld_out, R.H, R.hvec != 0,
+                      threadIdx.x & 31, e);
+  }
+  if (e) raise_err(P.err, e);
+}
+
 // The CTA that completed request r's race row in the fused launch: the verify outputs (as
 // write_request) and the final token at slot a_r of the drafter batch, at the first slot the
 // rebuild CTA published (long before any race row completes; the wait is bounded by time all
@@ -1398,7 +1460,12 @@ __device__ __noinline__ void fused_finish(const VerifyParams& P, int r, int a, i
     if (P.p_at) P.p_at[(size_t)r * K + t] = Ps[t];
     if (P.q_at) P.q_at[(size_t)r * K + t] = Qs[t];
   }
-  if (t == 0) {
+  if (t == 0 && P.fuse == 2) {
+    // the padded layout: request r's row a_r is r*2K + a_r, no published slot to wait for
+    P.num_accepted[r] = a;
+    P.rb.input_ids[(size_t)r * 2 * K + a] = (int32_t)b;
+    raise_err(P.err, e);
+  } else if (t == 0) {
     P.num_accepted[r] = a;
     unsigned* slot = &P.slots[r].off1;
     unsigned v = off_pre;
@@ -1504,7 +1571,8 @@ __global__ void __launch_bounds__(NT, min_blocks(DT))
       // [B, grid) race, dealt out to the requests as evenly as they go (request r takes race
       // CTAs [floor(r G / B), floor((r+1) G / B)) of the G = grid - B)
       if (blockIdx.x < (unsigned)P.B) {
-        rebuild_role(P, (int)blockIdx.x, sm);
+        if (P.fuse == 2) padded_rebuild_role(P, (int)blockIdx.x, sm);
+        else rebuild_role(P, (int)blockIdx.x, sm);
         return;
       }
       const uint64_t G = gridDim.x - (uint64_t)P.B, Bq = (uint64_t)P.B;
@@ -1996,7 +2064,7 @@ static int verify_launch_impl(int B, int K, int V, int dtype, const void* target
   P.cluster_blocks = B * P.nc;  // (unused when the race kernel takes the batch)
   P.vec = ((uintptr_t)target % 16 == 0) && ((uintptr_t)draft % 16 == 0) &&
           ((ld_t * esize) % 16 == 0) && ((ld_d * esize) % 16 == 0);
-  P.fuse = rb != nullptr && shape.fusable;
+  P.fuse = (rb != nullptr && shape.fusable) ? (rb->padded ? 2 : 1) : 0;
   P.wait_ns = wait_ns;
   P.withhold = withhold;
   if (P.fuse) {
@@ -2088,7 +2156,7 @@ static int verify_prepare_impl(
     const void* target_hidden, long ld_in, int n_in_rows, const void* h_shared, void* out_hidden,
     long ld_out, void* workspace, int32_t* err, cudaStream_t stream, uint64_t wait_ns,
     int withhold) {
-  sdk::RebuildArgs rb;
+  sdk::RebuildArgs rb = {};
   rb.pos0 = pos0;
   rb.block_table = block_table;
   rb.max_blocks = max_blocks;
@@ -2125,6 +2193,68 @@ static int verify_prepare_impl(
                         hidden_map, is_masked, is_rejected, start_loc, new_token_idx, total_out,
                         H, target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
                         stream);
+}
+
+extern "C" int sd_prep_padded_launch(int B, int K, const int32_t* out_tokens,
+                                     const int32_t* num_accepted, const int32_t* pos0,
+                                     const int32_t* block_table, int max_blocks, int block_size,
+                                     int32_t mask_token_id, int32_t* input_ids,
+                                     int32_t* positions, int32_t* slot_mapping,
+                                     int32_t* hidden_map, uint8_t* is_masked, uint8_t* rejected,
+                                     int32_t* scatter_map, int32_t* new_token_idx, int H,
+                                     const void* target_hidden, long ld_in, int n_in_rows,
+                                     const void* h_shared, void* out_hidden, long ld_out,
+                                     int32_t* err, cudaStream_t stream);
+
+// Verify and the padded drafter-batch rebuild in one call: one launch when the batch takes the
+// one-wave all-sampled path (each rebuild CTA recomputes its own request's decisions; the race
+// writes the final token at its fixed row), else the verify kernel and then the padded rebuild
+// kernel (the same outputs either way).
+extern "C" int sd_verify_prepare_padded_launch(
+    int B, int K, int V, int dtype, const void* target, long ld_t, const void* draft, long ld_d,
+    const int32_t* drafts, const float* temperature, uint64_t seed, uint32_t request_base,
+    int32_t* out_tokens, int32_t* num_accepted, float* p_at_draft, float* q_at_draft,
+    const int32_t* pos0, const int32_t* block_table, int max_blocks, int block_size,
+    int32_t mask_token_id, int32_t* input_ids, int32_t* positions, int32_t* slot_mapping,
+    int32_t* hidden_map, uint8_t* is_masked, uint8_t* rejected, int32_t* scatter_map,
+    int32_t* new_token_idx, int H, const void* target_hidden, long ld_in, int n_in_rows,
+    const void* h_shared, void* out_hidden, long ld_out, void* workspace, int32_t* err,
+    cudaStream_t stream) {
+  sdk::RebuildArgs rb = {};
+  rb.padded = 1;
+  rb.pos0 = pos0;
+  rb.block_table = block_table;
+  rb.max_blocks = max_blocks;
+  rb.block_size = block_size;
+  rb.mask_id = mask_token_id;
+  rb.input_ids = input_ids;
+  rb.positions = positions;
+  rb.slot_mapping = slot_mapping;
+  rb.hidden_map = hidden_map;
+  rb.is_masked = is_masked;
+  rb.rejected = rejected;
+  rb.scatter_map = scatter_map;
+  rb.new_token_idx = new_token_idx;
+  rb.H = H;
+  rb.hidden = (const uint16_t*)target_hidden;
+  rb.ld_in = ld_in;
+  rb.n_in_rows = n_in_rows;
+  rb.h_shared = (const uint16_t*)h_shared;
+  rb.out_hidden = (uint16_t*)out_hidden;
+  rb.ld_out = ld_out;
+  rb.hvec = out_hidden && (H % 8 == 0) && ((uintptr_t)target_hidden % 16 == 0) &&
+            ((uintptr_t)h_shared % 16 == 0) && ((uintptr_t)out_hidden % 16 == 0) &&
+            (ld_in % 8 == 0) && (ld_out % 8 == 0);
+  bool fused = false;
+  int rc = verify_launch_impl(B, K, V, dtype, target, ld_t, draft, ld_d, drafts, nullptr,
+                              temperature, seed, request_base, out_tokens, num_accepted,
+                              p_at_draft, q_at_draft, workspace, err, stream, &rb, &fused);
+  if (rc != SD_OK || fused) return rc;
+  return sd_prep_padded_launch(B, K, out_tokens, num_accepted, pos0, block_table, max_blocks,
+                               block_size, mask_token_id, input_ids, positions, slot_mapping,
+                               hidden_map, is_masked, rejected, scatter_map, new_token_idx, H,
+                               target_hidden, ld_in, n_in_rows, h_shared, out_hidden, ld_out, err,
+                               stream);
 }
 
 #define SD_VERIFY_PREPARE_PARAMS                                                                \
