@@ -21,13 +21,18 @@
 //    which GB300 executes slowly, so each thread filters with an fp32 approximation (one
 //    hardware lg2) and keeps only elements whose approximate key lies within a relative band
 //    of its running best; the CTA then evaluates the exact key r / fp32(-log(v)) for the few
-//    candidates. The band is 16x the exhaustively measured worst error of the approximation,
-//    so the winner (including the lowest-index rule on exact ties) is always among the
-//    candidates. A per-unit upper bound against the CTA's running best skips units that cannot
-//    hold a candidate.
-//  * Logit rows (bf16): per row the cluster forms max and sum of exp2((l - M) * log2(e)/T) for
-//    the target and draft rows together, decides the draft, and on rejection races on the same
-//    rows again (the second read is served from L2).
+//    candidates. The band is 23x twice the exhaustively measured worst error of the
+//    approximation, so the winner (including the lowest-index rule on exact ties) is always
+//    among the candidates. A per-unit upper bound against the CTA's running best skips units
+//    that cannot hold a candidate.
+//  * Logit rows (bf16): per row the cluster forms the sums of 2^(l c - ref c) (c = log2(e)/T_r,
+//    ref the draft token's logit: no running maximum) for the target and draft rows together,
+//    exchanges them while the next row's first quarter streams, decides the draft, and on
+//    rejection races on the same row pair (the target unit re-read for the skip bound, the
+//    draft unit only for the units that pass it).
+//  * sd_verify_prepare and sd_verify_prepare_padded fold the drafter-batch rebuild into the
+//    launch of an all-sampled one-wave batch: B extra CTAs recompute the accept decisions and
+//    write the drafter rows while the others race; only the final token comes from the race.
 //  * Per-request draft counts (a prefix of the counts) address each request's packed rows; the
 //    drafter-side sampler (sample_kernel) races each drafter row on its own Philox stream, in the
 //    log domain for logit rows (one pass: the softmax normaliser cancels).
