@@ -215,7 +215,8 @@ __device__ __forceinline__ float race_E_exact(uint32_t w) {
 // in 2048) the hardware lg2 loses relative accuracy, so there -log2(v) is formed from m = 1 - v
 // by its series instead. The scale 2^64 keeps r * R in the normal range for every positive fp32
 // residual r <= 2^30. The worst relative error of R against 2^64 / (E * log2(e)) over all 2^32
-// words is measured exhaustively by sd_race_E_approx_error; the race filter's band (2^-7) is 47x wider.
+// words is measured exhaustively by sd_race_E_approx_error; the race filter's band (2^-7) is 47x
+// wider.
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kNearOne = 0xFFE00000u;  // w >= this: 1 - v < 2^-11
 
