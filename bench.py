@@ -40,11 +40,11 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "c81fb81db8351602"): (90.737152e6, "ncu --set full, one fused launch of the full "
+    ("b64", "3ef34d017e8b1fca"): (90.967552e6, "ncu --set full, one fused launch of the full "
                                                "batch (one input set)"),
-    ("b256mix", "c81fb81db8351602"): (434.83392e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "c81fb81db8351602"): (785.671509e6, "ncu --set full at B=192, scaled x512/192"),
-    ("b1024lg", "c81fb81db8351602"): (3702.97242e6, "ncu --set full at B=96, scaled x1024/96"),
+    ("b256mix", "3ef34d017e8b1fca"): (434.304000e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "3ef34d017e8b1fca"): (784.706901e6, "ncu --set full at B=192, scaled x512/192"),
+    ("b1024lg", "3ef34d017e8b1fca"): (3707.142144e6, "ncu --set full at B=96, scaled x1024/96"),
 }
 
 
