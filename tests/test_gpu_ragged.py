@@ -74,9 +74,13 @@ def test_probability_rows_bit_exact(B, K_max, V, greedy, temp, seed):
     assert_verify_equal(got, want)
 
 
-def test_logit_rows_within_tolerance():
-    rng = np.random.default_rng(77)
-    B, K_max, V = 16, 6, 30011
+@pytest.mark.parametrize("B,V,seed", [
+    (16, 30011, 77),
+    (200, 40009, 78),  # enough requests for clusters of 4 CTAs per request
+])
+def test_logit_rows_within_tolerance(B, V, seed):
+    rng = np.random.default_rng(seed)
+    K_max = 6
     ks = rng.integers(0, K_max + 1, B)
     cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
     n = int(cu[-1])

@@ -87,7 +87,8 @@ def new_ws(w, dtype=sd.SD_F32_PROBS):
     ("b64", 64, True, 2),        # per-request temperatures
     ("b256mix", 32, True, 2),    # greedy requests among them
     ("b512rag", 200, False, 2),  # two waves: the race kernel, then the rebuild kernel
-    ("b1024lg", 24, True, 2),    # logit rows
+    ("b1024lg", 24, True, 2),    # logit rows, clusters of 8
+    ("b1024lg", 192, True, 2),   # logit rows, clusters of 4
 ])
 def test_same_bytes_as_the_two_calls(name, B, temp, kernels):
     w = workloads.make(name, device="cuda", B=B)
@@ -103,9 +104,15 @@ def test_same_bytes_as_the_two_calls(name, B, temp, kernels):
     assert int(got["err"].item()) == 0
 
 
-def test_rows_match_the_oracle():
-    w = workloads.make("b64", device="cuda", B=24)
-    got = run_one_call(w, None, new_ws(w))
+@pytest.mark.parametrize("name,B,temp", [
+    ("b64", 24, False),      # the single launch of rebuild CTAs and race CTAs
+    ("b256mix", 32, True),   # verify kernel then the padded rebuild kernel
+    ("b1024lg", 24, True),   # the same on logit rows
+])
+def test_rows_match_the_oracle(name, B, temp):
+    w = workloads.make(name, device="cuda", B=B)
+    dtype = sd.SD_BF16_LOGITS if w.kind == "logits" else sd.SD_F32_PROBS
+    got = run_one_call(w, w.temperature if temp else None, new_ws(w, dtype))
     bits = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     want = oracle.pdraft_prepare_padded(got["out_tokens"].cpu().numpy(),
                                         got["num_accepted"].cpu().numpy(), w.pos0.cpu().numpy(),
@@ -117,8 +124,10 @@ def test_rows_match_the_oracle():
     assert want["err"] == 0
 
 
-def test_error_paths_match_the_two_calls():
-    w = workloads.make("b64", device="cuda", B=32)
+@pytest.mark.parametrize("name", ["b64", "b1024lg"])
+def test_error_paths_match_the_two_calls(name):
+    w = workloads.make(name, device="cuda", B=32)
+    dtype = sd.SD_BF16_LOGITS if w.kind == "logits" else sd.SD_F32_PROBS
     table = w.block_table.clone()
     table[3, :] = -1                      # request 3's live slots miss the table
     n_in = w.B * (w.K + 1) - 5            # the last request's late hidden rows are missing
@@ -127,7 +136,7 @@ def test_error_paths_match_the_two_calls():
     w.drafts[6, 0] = w.V                  # request 6: its first draft is out of range
     for T in (None, w.temperature):
         want = run_two_calls(w, T, hidden=hidden, table=table)
-        got = run_one_call(w, T, new_ws(w), hidden=hidden, table=table)
+        got = run_one_call(w, T, new_ws(w, dtype), hidden=hidden, table=table)
         assert_same(got, want)
         err = int(got["err"].item())
         assert err & sd.SD_ERR_BLOCK_TABLE and err & sd.SD_ERR_TOKEN_RANGE
