@@ -74,6 +74,7 @@ def logit_case(rng, B, K, V, sigma=0.5, tlo=0.5, thi=1.2, greedy_frac=0.0):
     (12, 8, 201088, 0.2, 2),
     (40, 3, 777, 0.5, 3),
     (200, 3, 50001, 0.2, 4),  # enough requests for clusters of 4 CTAs (B * 4 CTAs fill a wave)
+    (192, 16, 40009, 0.1, 5),  # K = SD_K_MAX with clusters of 4
 ])
 def test_logits_within_tolerance(B, K, V, greedy, seed):
     rng = np.random.default_rng(200 + seed)
