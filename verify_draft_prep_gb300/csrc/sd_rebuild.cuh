@@ -50,7 +50,9 @@ __device__ __forceinline__ void write_padding_slot(long long i, int32_t* input_i
 }
 
 // One warp copies a row of nv 16-byte words: each lane issues all of its loads (up to
-// kCopyBatch) before its stores, so a row of a few KB costs one memory round trip.
+// kCopyBatch) before its stores, so a row of a few KB costs one memory round trip. The stores
+// are streaming (evict-first): the rows are written once and read by a later kernel, so they
+// leave L2 while this kernel runs instead of being written back during the next one's reads.
 constexpr int kCopyBatch = 12;
 __device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src,
                                               uint4* __restrict__ dst, int nv, int lane) {
@@ -61,7 +63,7 @@ __device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src,
       if (v0 + 32 * k < nv) x[k] = __ldg(src + v0 + 32 * k);
 #pragma unroll
     for (int k = 0; k < kCopyBatch; ++k)
-      if (v0 + 32 * k < nv) dst[v0 + 32 * k] = x[k];
+      if (v0 + 32 * k < nv) __stcs(dst + v0 + 32 * k, x[k]);
   }
 }
 
