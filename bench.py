@@ -40,11 +40,11 @@ L2_BYTES = 129 * 1024 * 1024
 # Captures of a reduced batch are scaled to the full batch by the units processed (the kernels'
 # traffic grows in proportion to the requests).
 MEASURED_TRAFFIC = {
-    ("b64", "53335dcf4efc0049"): (90.759424e6, "ncu --set full, one fused launch of the full "
+    ("b64", "c8fd3a12768eb5f3"): (90.784256e6, "ncu --set full, one fused launch of the full "
                                                "batch (one input set)"),
-    ("b256mix", "53335dcf4efc0049"): (434.572800e6, "ncu --set full at B=128, scaled x2"),
-    ("b512rag", "53335dcf4efc0049"): (783.996928e6, "ncu --set full at B=192, scaled x512/192"),
-    ("b1024lg", "53335dcf4efc0049"): (3669.798912e6, "ncu --set full at B=192, scaled x1024/192"),
+    ("b256mix", "c8fd3a12768eb5f3"): (432.580096e6, "ncu --set full at B=128, scaled x2"),
+    ("b512rag", "c8fd3a12768eb5f3"): (784.234496e6, "ncu --set full at B=192, scaled x512/192"),
+    ("b1024lg", "c8fd3a12768eb5f3"): (3670.736896e6, "ncu --set full at B=192, scaled x1024/192"),
 }
 
 
